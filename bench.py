@@ -1,0 +1,468 @@
+#!/usr/bin/env python3
+"""Benchmark of the MLA hot path on B300: one decode step of the V2-shaped batch-16,
+context-4096 workload (append the 16 new tokens' latent rows, project their queries,
+weight-absorbed decode over the latent cache), plus the causal-prefill workload.
+
+Prints ONE JSON line. ``--impl reference`` times the float64 CPU oracle instead (the
+baseline arm). Under torchrun every rank runs its own replica of the workload (decode
+sequences are independent; no data-path collective) and rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mla_inputs as mi  # noqa: E402
+
+ROW_BYTES_BF16 = (512 + 64) * 2
+DEFAULT_WORKLOAD = "v2_decode_b16_l4096"
+PREFILL_WORKLOAD = "v2_prefill_b2_t4096"
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------- accounting
+def decode_kernel_costs(wl: mi.Workload):
+    """Algorithmic bytes and flops of each kernel of one decode step (inputs read once,
+    outputs written once; split partials and other scratch traffic are not counted)."""
+    d = wl.dims
+    e = 2 if wl.dtype == "bf16" else 4
+    B = wl.B
+    rows = wl.n_rows
+    nc, nr = d.n_h * d.d_hc, d.n_h * d.d_hr
+    out = {
+        "append": dict(bytes=(d.row * d.d + B * d.d + B * d.row) * e,
+                       flops=2 * B * d.d * d.row),
+        "q_down": dict(bytes=(d.d_cq * d.d + B * d.d) * e + B * d.d_cq * 4,
+                       flops=2 * B * d.d * d.d_cq),
+        "q_up": dict(bytes=(nc + nr) * d.d_cq * e + B * d.d_cq * 4 + B * (nc + nr) * e,
+                     flops=2 * B * d.d_cq * (nc + nr)),
+        "absorb": dict(bytes=nc * d.d_c * e + B * nc * e + B * d.n_h * d.d_c * e,
+                       flops=2 * B * d.n_h * d.d_hc * d.d_c),
+        "decode_attn": dict(bytes=rows * d.row * e + B * d.n_h * (d.d_c + d.d_hr) * e,
+                            flops=rows * (2 * d.n_h * d.row + 2 * d.n_h * d.d_c)),
+        "decode_combine": dict(bytes=nc * d.d_c * e + B * d.n_h * d.d_hc * 4,
+                               flops=2 * B * d.n_h * d.d_hc * d.d_c),
+    }
+    return out
+
+
+def prefill_flops(wl: mi.Workload):
+    d = wl.dims
+    n = wl.n_rows
+    attn = sum(d.n_h * T * (T + 1) // 2 * 2 * (d.d_h + d.d_hc) for T in wl.seq_lens)
+    proj = 2 * n * d.d * (d.d_cq + d.row) + 2 * n * d.d_cq * d.n_h * (d.d_hc + d.d_hr)
+    expand = 2 * n * d.d_c * d.n_h * d.d_hc * 2
+    return attn, proj + expand
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        p = json.load(open(path))
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["unsampled"]}
+        loaded = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_decode_sample(wl: mi.Workload, budget_s: float):
+    """Time the float64 oracle on whole sequences of the decode workload (the new token's
+    latent row and query, then explicit per-head decode over all L rows) until about
+    ``budget_s`` seconds of CPU work; returns cache GB/s and the sample description."""
+    from oracle import mla_ref as ref
+    d = wl.dims
+    W = {k: v.astype(np.float64) for k, v in mi.weights(d, wl.dtype).items()}
+    done_rows, spent, seqs = 0, 0.0, 0
+    for b, L in enumerate(wl.seq_lens):
+        h = mi.hidden(d, wl.dtype, b, L, wl.seed)
+        c, kr = ref.kv_latent(h[:-1], W["W_DKV"], W["W_KR"], np.arange(L - 1), d.rope_base)
+        ctx = ref.store(ref.cache_rows(c, kr), wl.dtype)            # cache fill: not timed
+        t0 = time.perf_counter()
+        c1, kr1 = ref.kv_latent(h[-1:], W["W_DKV"], W["W_KR"], [L - 1], d.rope_base)
+        rows = np.concatenate([ctx, ref.store(ref.cache_rows(c1, kr1), wl.dtype)])
+        q_c, q_r = ref.query(h[-1:], W["W_DQ"], W["W_UQ"], W["W_QR"], [L - 1], d.n_h, d.d_hc,
+                             d.d_hr, d.rope_base)
+        ref.decode_explicit(ref.store(q_c, wl.dtype), ref.store(q_r, wl.dtype), [rows],
+                            W["W_UK"], W["W_UV"], d.d_c)
+        spent += time.perf_counter() - t0
+        done_rows += L
+        seqs += 1
+        if spent >= budget_s:
+            break
+    gbs = done_rows * d.row * (2 if wl.dtype == "bf16" else 4) / spent / 1e9
+    return gbs, spent, "%d of %d sequences (%d cache rows), all %d heads" % (
+        seqs, wl.B, done_rows, d.n_h)
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        return int(max(n)) if n else os.cpu_count()
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    wl = mi.workload(args.workload)
+    per_step_budget = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_decode_sample(wl, 0.0)
+    vals, times, sample = [], [], ""
+    for _ in range(args.steps):
+        v, t, sample = oracle_decode_sample(wl, per_step_budget)
+        vals.append(v)
+        times.append(t)
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": metric_name(), "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.mean(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def metric_name():
+    return "MLA decode cache GB/s + TFLOP/s (% roofline) on 1 B300; prefill TFLOP/s"
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "B": wl.B, "context": int(max(wl.seq_lens)),
+            "cache_rows": wl.n_rows, "dims": "d=5120 n_h=128 d_hc=128 d_hr=64 d_c=512 d_cq=1536",
+            "step": "append B new rows + project B queries + absorbed decode",
+            "l2": "flushed between timed steps (256 MB write)"}
+
+
+def setup_decode(wl, dev):
+    import torch
+    from mla_latent_kv_75_b300 import host
+    d = wl.dims
+    W = mi.weights(d, wl.dtype)
+    model = host.DeviceModel.upload(d, wl.dtype, W, dev)
+    base = mi.packed_layout(wl.seq_lens)
+    cache = host.LatentCache(d, wl.dtype, base, wl.n_rows, device=dev)
+    host.fill_context(model, cache, lambda b, n: mi.hidden(d, wl.dtype, b, n, wl.seed),
+                      wl.seq_lens)
+    step = host.DecodeStep(model, cache, wl.seq_lens)
+    h_new = np.stack([mi.hidden_rows(d, wl.dtype, b, [L - 1], wl.seed)[0]
+                      for b, L in enumerate(wl.seq_lens)])
+    h_dev = host.to_device(h_new, wl.dtype, dev)
+    h_host = host.to_device(h_new, wl.dtype, "cpu", pin=True)
+    o_host = torch.empty(step.o.shape, dtype=step.o.dtype).pin_memory()
+    torch.cuda.synchronize()
+    return step, h_dev, h_host, o_host
+
+
+def time_steps(fn, steps, flush, trace_capacity=0):
+    """Run ``steps`` steps, each bracketed by CUDA events on the current stream, with an L2
+    flush before each (outside the events). Returns per-step ms and the kernel trace."""
+    import torch
+    import mla_latent_kv_75_b300 as mla
+    st = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    trace = mla.KernelTrace(trace_capacity) if trace_capacity else None
+    if trace:
+        trace.__enter__()
+    for k in range(steps):
+        flush()
+        evs[k][0].record(st)
+        fn()
+        evs[k][1].record(st)
+    if trace:
+        trace.__exit__(None, None, None)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    return ms, (trace.launches() if trace else [])
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import mla_latent_kv_75_b300 as mla
+    from mla_latent_kv_75_b300 import host
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = mi.workload(args.workload)
+    peaks = load_peaks()
+    step, h_dev, h_host, o_host = setup_decode(wl, dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    def one_step():
+        step.step(h_dev)
+
+    def one_e2e():
+        h_dev.copy_(h_host, non_blocking=True)
+        step.step(h_dev)
+        o_host.copy_(step.o, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        flush()
+        one_step()
+    assert mla.mla_get_device_status() == 0
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms, launches = time_steps(one_step, args.steps, flush, trace_capacity=64 * args.steps)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = sum(ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clocks = clk.summary()
+    ms_step = total_ms / args.steps
+
+    for _ in range(3):
+        flush()
+        one_e2e()
+    e2e_ms, _ = time_steps(one_e2e, args.steps, flush)
+    e2e_total = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+
+    costs = decode_kernel_costs(wl)
+    e = 2 if wl.dtype == "bf16" else 4
+    cache_bytes = wl.n_rows * wl.dims.row * e
+    step_flops = sum(c["flops"] for c in costs.values())
+    value = world * cache_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    e2e_value = world * cache_bytes * args.steps / (e2e_total * 1e-3) / 1e9
+
+    # per-kernel breakdown from the launch trace
+    per = {}
+    for name, t in launches:
+        per.setdefault(name, []).append(t)
+    kernels = {}
+    for name, ts in per.items():
+        avg_ms = statistics.mean(ts)
+        c = costs.get(name)
+        entry = {"launches": len(ts), "avg_us": round(avg_ms * 1e3, 3),
+                 "share": round(sum(ts) / sum(sum(v) for v in per.values()), 4)}
+        if c:
+            gbs = c["bytes"] / (avg_ms * 1e-3) / 1e9
+            tfl = c["flops"] / (avg_ms * 1e-3) / 1e12
+            floor_s = max(c["bytes"] / (peaks["hbm_gbs"] * 1e9),
+                          c["flops"] / (peaks["bf16_tflops"] * 1e12))
+            entry.update({"alg_bytes": c["bytes"], "alg_flops": c["flops"],
+                          "GB_s": round(gbs, 1), "TFLOP_s": round(tfl, 2),
+                          "roofline_frac": round(floor_s / (avg_ms * 1e-3), 4)})
+        kernels[name] = entry
+    dominant = max(per, key=lambda n: sum(per[n])) if per else None
+    roofline = None
+    if dominant and dominant in costs:
+        c = costs[dominant]
+        avg_s = statistics.mean(per[dominant]) * 1e-3
+        ai = c["flops"] / c["bytes"]
+        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        if ai < ridge:
+            achieved = c["bytes"] / avg_s / 1e9
+            roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1),
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(achieved / peaks["hbm_gbs"], 4)}
+        else:
+            achieved = c["flops"] / avg_s / 1e12
+            roofline = {"kernel": dominant, "bound": "tensor", "achieved": round(achieved, 2),
+                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": round(achieved / peaks["bf16_tflops"], 4)}
+        roofline["peak_source"] = peaks["source"]
+        roofline["traffic"] = None
+
+    # the absorbed-decode call alone (absorb + attention + combine)
+    dec_names = ("absorb", "decode_attn", "decode_combine")
+    dec_s = sum(statistics.mean(per[n]) for n in dec_names if n in per) * 1e-3
+    dec_bytes = sum(costs[n]["bytes"] for n in dec_names)
+    dec_flops = sum(costs[n]["flops"] for n in dec_names)
+    decode_call = None
+    if dec_s > 0:
+        floor_s = max(dec_bytes / (peaks["hbm_gbs"] * 1e9), dec_flops / (peaks["bf16_tflops"] * 1e12))
+        decode_call = {"us": round(dec_s * 1e6, 2), "cache_GB_s": round(cache_bytes / dec_s / 1e9, 1),
+                       "TFLOP_s": round(dec_flops / dec_s / 1e12, 2),
+                       "roofline_frac": round(floor_s / dec_s, 4)}
+
+    prefill = None
+    if not args.no_prefill:
+        prefill = run_prefill(args, dev, peaks, flush)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, spent, sample = oracle_decode_sample(wl, args.cpu_seconds)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": sample, "seconds": round(spent, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": metric_name(), "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": workload_config(wl),
+            "tflops": round(world * step_flops * args.steps / (total_ms * 1e-3) / 1e12, 3),
+            "roofline": roofline, "decode_call": decode_call, "kernels": kernels,
+            "prefill": prefill, "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": int(h_host.numel() * h_host.element_size()),
+                    "d2h_bytes_per_step": int(o_host.numel() * o_host.element_size()),
+                    "ms_per_step": round(e2e_total / args.steps, 4)},
+            "gpu_launches": len(launches), "clocks": clocks,
+            "fast_path": mla.mla_fast_path(step.model.abi_dims),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_prefill(args, dev, peaks, flush):
+    import torch
+    from mla_latent_kv_75_b300 import host
+    import mla_latent_kv_75_b300 as mla
+    wl = mi.workload(PREFILL_WORKLOAD)
+    d = wl.dims
+    W = mi.weights(d, wl.dtype)
+    model = host.DeviceModel.upload(d, wl.dtype, W, dev)
+    cache = host.LatentCache(d, wl.dtype, mi.packed_layout(wl.seq_lens), wl.n_rows, device=dev)
+    pre = host.PrefillStep(model, cache, wl.seq_lens)
+    h = host.to_device(np.concatenate([mi.hidden(d, wl.dtype, b, L, wl.seed)
+                                       for b, L in enumerate(wl.seq_lens)]), wl.dtype, dev)
+    steps = max(1, min(args.steps, args.prefill_steps))
+    for _ in range(3):
+        pre.run(h)
+    assert mla.mla_get_device_status() == 0
+    ms, launches = time_steps(lambda: pre.run(h), steps, flush, trace_capacity=16 * steps)
+    attn_f, other_f = prefill_flops(wl)
+    per = {}
+    for name, t in launches:
+        per.setdefault(name, []).append(t)
+    attn_ms = statistics.mean(per["prefill_attn"]) if "prefill_attn" in per else None
+    step_ms = statistics.mean(ms)
+    out = {"workload": wl.name, "ms_per_step": round(step_ms, 3),
+           "TFLOP_s": round((attn_f + other_f) / (step_ms * 1e-3) / 1e12, 2),
+           "attn_TFLOP_s": round(attn_f / (attn_ms * 1e-3) / 1e12, 2) if attn_ms else None,
+           "attn_frac_of_peak": round(attn_f / (attn_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)
+           if attn_ms else None,
+           "kernels_us": {n: round(statistics.mean(v) * 1e3, 1) for n, v in per.items()}}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

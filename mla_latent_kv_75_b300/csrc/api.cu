@@ -1,0 +1,223 @@
+// C ABI of libmla: argument validation, workspace sizing and dispatch to the kernel files.
+// The operations are those of "MLA前向计算流程" §三分支计算 ①–④ (see include/mla.h).
+#include <stdio.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace mla;
+
+namespace {
+
+mla_status_t check_dims(const mla_dims_t* d) {
+  if (!d) return MLA_ERR_INVALID_ARG;
+  if (d->d <= 0 || d->n_h <= 0 || d->d_hc <= 0 || d->d_hr <= 0 || d->d_c <= 0 || d->d_cq <= 0)
+    return MLA_ERR_INVALID_ARG;
+  if (d->dtype != MLA_F32 && d->dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+  if (!(d->rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
+  // RoPE rotates pairs; the pair-wise epilogues need even content widths too.
+  if ((d->d_hr & 1) || (d->d_c & 1) || (d->d_hc & 1)) return MLA_ERR_UNSUPPORTED;
+  // vectorised row access: 16-byte row pitches of the cache and of every weight row
+  const int v = d->dtype == MLA_BF16 ? 8 : 4;
+  if ((d->d_c + d->d_hr) % v || d->d % v || d->d_cq % v || d->d_c % v) return MLA_ERR_UNSUPPORTED;
+  // SIMT kernels stage a handful of rows in shared memory
+  if (simt_decode_smem(d) > 200 * 1024 || simt_prefill_smem(d) > 200 * 1024)
+    return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+mla_status_t check_ptr(const void* p) {
+  if (!p) return MLA_ERR_INVALID_ARG;
+  return aligned16(p) ? MLA_OK : MLA_ERR_MISALIGNED;
+}
+
+#define MLA_TRY(x)                       \
+  do {                                   \
+    mla_status_t s_ = (x);               \
+    if (s_ != MLA_OK) return s_;         \
+  } while (0)
+
+}  // namespace
+
+// ------------------------------------------------------------------ launch tracing
+namespace mla {
+namespace {
+struct TraceState {
+  void* const* events = nullptr;
+  int32_t* ids = nullptr;
+  int32_t n_pairs = 0;
+  int32_t count = 0;
+  bool armed = false;
+};
+TraceState g_trace;
+const char* const kKernelNames[K_NUM_IDS] = {
+    "append", "q_down", "q_up", "absorb", "decode_attn", "decode_combine", "token_map",
+    "prefill_append", "prefill_q_down", "prefill_q_up", "expand_k", "expand_v", "prefill_attn"};
+}  // namespace
+
+void trace_before(int kernel_id, cudaStream_t st) {
+  if (!g_trace.armed || g_trace.count >= g_trace.n_pairs) return;
+  g_trace.ids[g_trace.count] = kernel_id;
+  cudaEventRecord((cudaEvent_t)g_trace.events[2 * g_trace.count], st);
+}
+
+void trace_after(cudaStream_t st) {
+  if (!g_trace.armed || g_trace.count >= g_trace.n_pairs) return;
+  cudaEventRecord((cudaEvent_t)g_trace.events[2 * g_trace.count + 1], st);
+  ++g_trace.count;
+}
+}  // namespace mla
+
+extern "C" {
+
+mla_status_t mla_trace_arm(void* const* events, int32_t* ids, int32_t n_pairs) {
+  if (n_pairs < 0 || (n_pairs > 0 && (!events || !ids))) return MLA_ERR_INVALID_ARG;
+  g_trace.events = events;
+  g_trace.ids = ids;
+  g_trace.n_pairs = n_pairs;
+  g_trace.count = 0;
+  g_trace.armed = n_pairs > 0;
+  return MLA_OK;
+}
+
+int32_t mla_trace_disarm(void) {
+  const int32_t n = g_trace.count;
+  g_trace = TraceState();
+  return n;
+}
+
+const char* mla_kernel_name(int32_t id) {
+  return (id >= 0 && id < K_NUM_IDS) ? kKernelNames[id] : "unknown";
+}
+
+int32_t mla_fast_path(const mla_dims_t* d) {
+  (void)d;
+  return 0;
+}
+
+mla_status_t mla_append_cache(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                              const int32_t* seq_idx, const int32_t* pos, int32_t n,
+                              mla_cache_t* cache, void* stream) {
+  MLA_TRY(check_dims(d));
+  if (!w || !cache || n < 0) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  if (!seq_idx || !pos || !cache->seq_base || cache->capacity < 0) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_ptr(h));
+  MLA_TRY(check_ptr(w->W_DKV));
+  MLA_TRY(check_ptr(w->W_KR));
+  MLA_TRY(check_ptr(cache->rows));
+  return simt_append(d, w, h, seq_idx, pos, n, cache, as_stream(stream));
+}
+
+mla_status_t mla_project_q_workspace_size(const mla_dims_t* d, int32_t n, size_t* bytes) {
+  MLA_TRY(check_dims(d));
+  if (!bytes || n < 0) return MLA_ERR_INVALID_ARG;
+  *bytes = simt_project_q_ws(d, n);
+  return MLA_OK;
+}
+
+mla_status_t mla_project_q(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                           const int32_t* pos, int32_t n, void* ws, size_t ws_bytes, void* q_c,
+                           void* q_r, void* stream) {
+  MLA_TRY(check_dims(d));
+  if (!w || n < 0) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  if (!pos) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_ptr(h));
+  MLA_TRY(check_ptr(w->W_DQ));
+  MLA_TRY(check_ptr(w->W_UQ));
+  MLA_TRY(check_ptr(w->W_QR));
+  MLA_TRY(check_ptr(q_c));
+  MLA_TRY(check_ptr(q_r));
+  size_t need = 0;
+  MLA_TRY(mla_project_q_workspace_size(d, n, &need));
+  if (need && (!ws || ws_bytes < need)) return MLA_ERR_WORKSPACE;
+  if (need) MLA_TRY(check_ptr(ws));
+  return simt_project_q(d, w, h, pos, n, ws, q_c, q_r, as_stream(stream));
+}
+
+mla_status_t mla_decode_workspace_size(const mla_dims_t* d, int32_t B, int32_t max_len,
+                                       size_t* bytes) {
+  MLA_TRY(check_dims(d));
+  if (!bytes || B < 0 || max_len < 0) return MLA_ERR_INVALID_ARG;
+  *bytes = simt_decode_ws(d, B, max_len);
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_absorbed(const mla_dims_t* d, const mla_weights_t* w, const void* q_c,
+                                 const void* q_r, const mla_cache_t* cache,
+                                 const int32_t* seq_len, int32_t B, int32_t max_len, void* ws,
+                                 size_t ws_bytes, float* o, void* stream) {
+  MLA_TRY(check_dims(d));
+  if (!w || !cache || B < 0 || max_len < 0) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!seq_len || !cache->seq_base || cache->capacity < 0) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_ptr(q_c));
+  MLA_TRY(check_ptr(q_r));
+  MLA_TRY(check_ptr(w->W_UK));
+  MLA_TRY(check_ptr(w->W_UV));
+  MLA_TRY(check_ptr(o));
+  if (max_len > 0) MLA_TRY(check_ptr(cache->rows));
+  size_t need = 0;
+  MLA_TRY(mla_decode_workspace_size(d, B, max_len, &need));
+  if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  MLA_TRY(check_ptr(ws));
+  return simt_decode(d, w, q_c, q_r, cache, seq_len, B, max_len, ws, o, as_stream(stream));
+}
+
+mla_status_t mla_prefill_workspace_size(const mla_dims_t* d, int32_t n_tok, int32_t B,
+                                        int32_t max_T, size_t* bytes) {
+  MLA_TRY(check_dims(d));
+  if (!bytes || n_tok < 0 || B < 0 || max_T < 0) return MLA_ERR_INVALID_ARG;
+  *bytes = simt_prefill_ws(d, n_tok);
+  return MLA_OK;
+}
+
+mla_status_t mla_prefill(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                         const int32_t* cu_seqlens, int32_t B, int32_t n_tok, int32_t max_T,
+                         mla_cache_t* cache, void* ws, size_t ws_bytes, float* o,
+                         void* stream) {
+  MLA_TRY(check_dims(d));
+  if (!w || !cache || B < 0 || n_tok < 0 || max_T < 0) return MLA_ERR_INVALID_ARG;
+  if (n_tok == 0 || B == 0) return MLA_OK;
+  if (!cu_seqlens || !cache->seq_base || cache->capacity < 0) return MLA_ERR_INVALID_ARG;
+  if ((int64_t)max_T * B < n_tok) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_ptr(h));
+  const void* mats[] = {w->W_DQ, w->W_UQ, w->W_QR, w->W_DKV, w->W_KR, w->W_UK, w->W_UV};
+  for (const void* p : mats) MLA_TRY(check_ptr(p));
+  MLA_TRY(check_ptr(cache->rows));
+  MLA_TRY(check_ptr(o));
+  size_t need = 0;
+  MLA_TRY(mla_prefill_workspace_size(d, n_tok, B, max_T, &need));
+  if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  MLA_TRY(check_ptr(ws));
+  return simt_prefill(d, w, h, cu_seqlens, B, n_tok, max_T, cache, ws, o, as_stream(stream));
+}
+
+mla_status_t mla_get_device_status(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return MLA_ERR_CUDA;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  return (mla_status_t)v;
+}
+
+const char* mla_status_string(mla_status_t s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported dimensions";
+    case MLA_ERR_CAPACITY: return "cache row outside [0, capacity)";
+    case MLA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_TIMEOUT: return "bounded device wait gave up";
+    case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MLA_ERR_LENGTH: return "sequence length above max_len";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+// Kernel ids for launch tracing (names in api.cu).
+enum KernelId : int {
+  K_APPEND = 0, K_Q_DOWN, K_Q_UP, K_ABSORB, K_DECODE_ATTN, K_DECODE_COMBINE, K_TOKEN_MAP,
+  K_PREFILL_APPEND, K_PREFILL_Q_DOWN, K_PREFILL_Q_UP, K_EXPAND_K, K_EXPAND_V, K_PREFILL_ATTN,
+  K_NUM_IDS
+};
+
+// Launch tracing (host side): while armed, trace_before/trace_after record caller-owned
+// CUDA events around each kernel launch on its stream.
+void trace_before(int kernel_id, cudaStream_t st);
+void trace_after(cudaStream_t st);
+
+// RAII helper placed around one kernel launch.
+struct TraceScope {
+  cudaStream_t st;
+  TraceScope(int id, cudaStream_t s) : st(s) { trace_before(id, s); }
+  ~TraceScope() { trace_after(st); }
+};
+
+// Portable SIMT kernels (simt.cu)
+mla_status_t simt_append(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                         const int32_t* seq_idx, const int32_t* pos, int n, mla_cache_t* cache,
+                         cudaStream_t st);
+size_t simt_project_q_ws(const mla_dims_t* d, int n);
+mla_status_t simt_project_q(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                            const int32_t* pos, int n, void* ws, void* q_c, void* q_r,
+                            cudaStream_t st);
+size_t simt_decode_ws(const mla_dims_t* d, int B, int max_len);
+size_t simt_decode_smem(const mla_dims_t* d);
+mla_status_t simt_decode(const mla_dims_t* d, const mla_weights_t* w, const void* q_c,
+                         const void* q_r, const mla_cache_t* cache, const int32_t* seq_len,
+                         int B, int max_len, void* ws, float* o, cudaStream_t st);
+size_t simt_prefill_ws(const mla_dims_t* d, int n_tok);
+size_t simt_prefill_smem(const mla_dims_t* d);
+mla_status_t simt_prefill(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                          const int32_t* cu, int B, int n, int max_T, mla_cache_t* cache,
+                          void* ws, float* o, cudaStream_t st);
+
+}  // namespace mla
