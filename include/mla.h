@@ -134,6 +134,31 @@ mla_status_t mla_decode_absorbed(const mla_dims_t* dims, const mla_weights_t* w,
                                  const int32_t* seq_len, int32_t B, int32_t max_len,
                                  void* ws, size_t ws_bytes, float* o, void* stream);
 
+/* Scratch capacity of mla_decode_absorbed_static, in bytes (32 MiB). */
+#define MLA_STATIC_WS_BYTES (32u << 20)
+
+/* mla_decode_absorbed without a caller-provided workspace. The pages have no counterpart:
+ * this entry point exists for callers that cannot allocate device memory themselves, for
+ * example a plugin running inside a host framework that owns every device allocation, or a
+ * loop that must not call cudaMalloc after start-up because cudaMalloc may synchronise the
+ * device. It computes exactly what mla_decode_absorbed computes, with the same kernels, but
+ * its scratch is a fixed MLA_STATIC_WS_BYTES array compiled into the library; every GPU that
+ * loads the library holds that array until the process exits. The caller still provides
+ * q_c, q_r, the cache, seq_len and the output o.
+ *  - Problems whose workspace (mla_decode_workspace_size) exceeds MLA_STATIC_WS_BYTES are
+ *    rejected with MLA_ERR_WORKSPACE before any launch.
+ *  - The first call on a device looks up the array's device address (once per device, with
+ *    that device current); make that first call before any stream capture begins.
+ *  - All calls share the one array, which keeps the previous call's contents; the decode
+ *    kernels overwrite every scratch byte they read, so nothing needs clearing. Calls whose
+ *    kernels overlap on the GPU (several streams, several host threads) race on the array:
+ *    serialise them.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
+mla_status_t mla_decode_absorbed_static(const mla_dims_t* dims, const mla_weights_t* w,
+                                        const void* q_c, const void* q_r,
+                                        const mla_cache_t* cache, const int32_t* seq_len,
+                                        int32_t B, int32_t max_len, float* o, void* stream);
+
 /* Workspace needed by mla_prefill for n_tok tokens in B sequences of at most max_T tokens. */
 mla_status_t mla_prefill_workspace_size(const mla_dims_t* dims, int32_t n_tok, int32_t B,
                                         int32_t max_T, size_t* bytes);

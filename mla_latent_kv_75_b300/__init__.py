@@ -4,7 +4,7 @@ A thin ctypes layer: every function has the name and argument order of the C ent
 declared in ``include/mla.h`` and only marshals arguments (torch tensors become device
 pointers, the current torch stream becomes the cudaStream_t). All arithmetic runs in the
 library's CUDA kernels. There is no CPU fallback: importing this package fails if the
-library has not been built (``python -m mla_latent_kv_75_b300.build``).
+library has not been built (``python mla_latent_kv_75_b300/build.py``).
 """
 from __future__ import annotations
 
@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmla.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError("libmla.so is not built; run `python -m mla_latent_kv_75_b300.build` "
+    raise ImportError("libmla.so is not built; run `python mla_latent_kv_75_b300/build.py` "
                       "(the CUDA library is required, there is no fallback)")
 
 _lib = ctypes.CDLL(LIB_PATH)
@@ -67,6 +67,7 @@ _SIGS = {
     "mla_decode_absorbed": [_PD, _PW, _P, _P, _PC, _P, _I, _I, _P, ctypes.c_size_t, _P, _P],
     "mla_prefill_workspace_size": [_PD, _I, _I, _I, _SZ],
     "mla_prefill": [_PD, _PW, _P, _P, _I, _I, _I, _PC, _P, ctypes.c_size_t, _P, _P],
+    "mla_decode_absorbed_static": [_PD, _PW, _P, _P, _PC, _P, _I, _I, _P, _P],
     "mla_get_device_status": [_P],
     "mla_fast_path": [_PD],
 }
@@ -166,6 +167,19 @@ def mla_decode_absorbed(dims, weights, q_c, q_r, cache, seq_len, B, max_len, ws,
                                     _ptr(q_r), ctypes.byref(cache), _ptr(seq_len), int(B),
                                     int(max_len), _ptr(ws), int(ws_bytes), _ptr(o),
                                     _stream(stream)), "mla_decode_absorbed")
+
+
+MLA_STATIC_WS_BYTES = 32 << 20
+
+
+def mla_decode_absorbed_static(dims, weights, q_c, q_r, cache, seq_len, B, max_len, o,
+                               stream=None) -> None:
+    """mla_decode_absorbed with the library's built-in scratch array instead of a caller
+    workspace (for callers that cannot allocate device memory)."""
+    _check(_lib.mla_decode_absorbed_static(ctypes.byref(dims), ctypes.byref(weights), _ptr(q_c),
+                                           _ptr(q_r), ctypes.byref(cache), _ptr(seq_len),
+                                           int(B), int(max_len), _ptr(o), _stream(stream)),
+           "mla_decode_absorbed_static")
 
 
 def mla_prefill_workspace_size(dims, n_tok, B, max_T) -> int:

@@ -1,7 +1,7 @@
 """Build libmla.so in-tree from the CUDA sources in csrc/ (sm_103a only).
 
 Each .cu file is compiled separately with relocatable device code, then device-linked into
-one shared library next to this file. Run ``python -m mla_latent_kv_75_b300.build``.
+one shared library next to this file. Run ``python mla_latent_kv_75_b300/build.py``.
 """
 from __future__ import annotations
 
