@@ -39,6 +39,15 @@ mla_status_t check_ptr(const void* p) {
 
 }  // namespace
 
+namespace mla {
+// The tensor-core kernels are specialised to the DeepSeek-V2 head widths (n_h 128, d_h^C 128,
+// d_h^R 64, d_c 512) in bf16; d and d_c' only need to be multiples of 64 / 128.
+bool fast_dims(const mla_dims_t* d) {
+  return d->dtype == MLA_BF16 && d->n_h == 128 && d->d_hc == 128 && d->d_hr == 64 &&
+         d->d_c == 512 && d->d % 64 == 0 && d->d_cq % 128 == 0;
+}
+}  // namespace mla
+
 // ------------------------------------------------------------------ launch tracing
 namespace mla {
 namespace {
@@ -91,8 +100,8 @@ const char* mla_kernel_name(int32_t id) {
 }
 
 int32_t mla_fast_path(const mla_dims_t* d) {
-  (void)d;
-  return 0;
+  if (check_dims(d) != MLA_OK) return 0;
+  return fast_dims(d) ? 1 : 0;
 }
 
 mla_status_t mla_append_cache(const mla_dims_t* d, const mla_weights_t* w, const void* h,
@@ -106,13 +115,16 @@ mla_status_t mla_append_cache(const mla_dims_t* d, const mla_weights_t* w, const
   MLA_TRY(check_ptr(w->W_DKV));
   MLA_TRY(check_ptr(w->W_KR));
   MLA_TRY(check_ptr(cache->rows));
+  if (fast_dims(d))
+    return tc_append(d, w, h, seq_idx, pos, n, cache, nullptr, K_APPEND, as_stream(stream));
   return simt_append(d, w, h, seq_idx, pos, n, cache, as_stream(stream));
 }
 
 mla_status_t mla_project_q_workspace_size(const mla_dims_t* d, int32_t n, size_t* bytes) {
   MLA_TRY(check_dims(d));
   if (!bytes || n < 0) return MLA_ERR_INVALID_ARG;
-  *bytes = simt_project_q_ws(d, n);
+  // fast path: c^Q as a hi/lo pair of bf16 matrices [n, d_c'] (c^Q = hi + lo to ~2^-16)
+  *bytes = fast_dims(d) ? 2 * align_up((size_t)n * d->d_cq * 2, 256) : simt_project_q_ws(d, n);
   return MLA_OK;
 }
 
@@ -133,6 +145,13 @@ mla_status_t mla_project_q(const mla_dims_t* d, const mla_weights_t* w, const vo
   MLA_TRY(mla_project_q_workspace_size(d, n, &need));
   if (need && (!ws || ws_bytes < need)) return MLA_ERR_WORKSPACE;
   if (need) MLA_TRY(check_ptr(ws));
+  if (fast_dims(d)) {
+    char* hi = (char*)ws;
+    char* lo = hi + align_up((size_t)n * d->d_cq * 2, 256);
+    MLA_TRY(tc_q_down(d, w, h, n, hi, lo, K_Q_DOWN, as_stream(stream)));
+    return tc_q_up(d, w, hi, lo, pos, n, q_c, q_r, (int64_t)d->n_h * d->d_hc, d->d_hc,
+                   (int64_t)d->n_h * d->d_hr, d->d_hr, false, K_Q_UP, as_stream(stream));
+  }
   return simt_project_q(d, w, h, pos, n, ws, q_c, q_r, as_stream(stream));
 }
 

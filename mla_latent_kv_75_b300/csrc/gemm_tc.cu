@@ -1,0 +1,318 @@
+// Tensor-core projection GEMM for the MLA projections ("MLA前向计算流程" §三分支计算 ①②③):
+//   Y[n, o] = sum_k W[o, k] * X[n, k]      (W stored [out, in], X one token per row)
+// computed as D[o, n] = A[o, :] . B[n, :] with A = W (M = output features) and B = X (N =
+// tokens), both K-major, bf16 in, fp32 accumulation in tensor memory. One CTA owns a 128 x BN
+// output tile: warp 0 streams 64-wide K slices of W and X into a shared-memory ring with TMA,
+// warp 1 issues tcgen05.mma, warps 2..5 read the accumulator from TMEM and run the epilogue
+// (RoPE on pairs of adjacent output rows, cache-row scatter, dtype conversion).
+#include "internal.h"
+#include "proj_tc.h"
+#include "tc.cuh"
+
+namespace mla {
+
+using namespace tc;
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kTileA = 128 * 128;  // 128 rows x 64 bf16
+
+template <int BN>
+struct ProjSmem {
+  static constexpr uint32_t kTileB = BN * 128;
+  static constexpr uint32_t kStage = kTileA + kTileB;
+  static constexpr uint32_t kBars = kStages * kStage;
+  static constexpr uint32_t kBytes = kBars + 256;
+};
+
+template <int BN, class Ep>
+__global__ void __launch_bounds__(kThreads, 1)
+    proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0,
+                     const __grid_constant__ CUtensorMap tm_w1,
+                     const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_x2, int m_tiles0, int O, int N,
+                     int k_chunks, int dual, Ep ep) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  using S = ProjSmem<BN>;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBars);
+  uint64_t* empty = full + kStages;
+  uint64_t* done = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x, n0 = blockIdx.y * BN;
+  const bool from_w1 = m_tile >= m_tiles0;
+  const int a_row = from_w1 ? (m_tile - m_tiles0) * 128 : m_tile * 128;
+  const int total_chunks = dual ? 2 * k_chunks : k_chunks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, BN < 32 ? 32 : BN);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    tma_prefetch(&tm_w0);
+    tma_prefetch(&tm_x);
+    int issued = 0;
+    for (int kc = 0; kc < total_chunks; ++kc) {
+      const int s = kc % kStages, r = kc / kStages;
+      if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort)) break;
+      uint8_t* a = smem + s * S::kStage;
+      uint8_t* b = a + kTileA;
+      mbar_arrive_expect_tx(&full[s], S::kStage);
+      const int kx = (kc % k_chunks) * 64;
+      tma_load_2d(a, from_w1 ? &tm_w1 : &tm_w0, &full[s], kx, a_row);
+      tma_load_2d(b, (dual && kc >= k_chunks) ? &tm_x2 : &tm_x, &full[s], kx, n0);
+      ++issued;
+    }
+    // drain: every issued copy must land before the CTA may exit
+    for (int kc = (issued > kStages ? issued - kStages : 0); kc < issued; ++kc)
+      mbar_wait(&full[kc % kStages], (kc / kStages) & 1, abort);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc = idesc_f16(128, BN, 1, 0, 0);
+    for (int kc = 0; kc < total_chunks; ++kc) {
+      const int s = kc % kStages, r = kc / kStages;
+      if (!mbar_wait(&full[s], r & 1, abort)) break;
+      tc_fence_after();
+      const uint32_t a = smem_u32(smem + s * S::kStage);
+      const uint32_t b = a + kTileA;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ss(tmem, smem_desc(a + kk * 32, 16, 1024), smem_desc(b + kk * 32, 16, 1024), idesc,
+               (kc | kk) != 0);
+      mma_commit(&empty[s]);
+    }
+    mma_commit(done);
+  } else if (warp >= 2) {
+    // ---------------- epilogue: TMEM -> registers -> global
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int o = (from_w1 ? m_tiles0 * 128 + a_row : a_row) + q * 32 + lane;
+    if (mbar_wait(done, 0, abort)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float vp = __shfl_xor_sync(0xffffffffu, v[j], 1);
+          const int n = n0 + c + j;
+          if (n < N && o < O) ep(o, n, v[j], vp);
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, BN < 32 ? 32 : BN);
+  }
+}
+
+// ------------------------------------------------------------------------- epilogues
+// Cache append: rows [0, d_c) of [W^DKV; W^KR] are c^KV, rows [d_c, d_c + d_hr) are k^R,
+// rotated by RoPE at the token's position. Optionally also stored to a packed copy.
+struct EpAppend {
+  __nv_bfloat16* rows;
+  int64_t pitch, capacity;
+  const int64_t* seq_base;
+  const int32_t* seq_idx;
+  const int32_t* pos;
+  __nv_bfloat16* packed;  // [N, pitch] or null
+  int d_c, d_hr;
+  float base;
+  __device__ void operator()(int o, int n, float v, float vp) const {
+    const int p = pos[n];
+    if (o >= d_c) {
+      float c, s;
+      rope_cs(p, (o - d_c) >> 1, d_hr, base, &c, &s);
+      v = ((o - d_c) & 1) ? (vp * s + v * c) : (v * c - vp * s);
+    }
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    const int64_t row = seq_base[seq_idx[n]] + p;
+    if (row < 0 || row >= capacity) {
+      flag_status(MLA_ERR_CAPACITY);
+    } else {
+      rows[row * pitch + o] = b;
+    }
+    if (packed) packed[(int64_t)n * pitch + o] = b;
+  }
+};
+
+// Plain store Y[n * ld + o] in bf16, or as a hi/lo pair of bf16 (v = hi + lo to ~2^-16).
+struct EpStoreBF16 {
+  __nv_bfloat16* hi;
+  __nv_bfloat16* lo;  // null: single bf16
+  int64_t ld;
+  __device__ void operator()(int o, int n, float v, float) const {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    hi[(int64_t)n * ld + o] = h;
+    if (lo) lo[(int64_t)n * ld + o] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+};
+
+struct EpStoreF16 {
+  __half* y;
+  int64_t ld;
+  __device__ void operator()(int o, int n, float v, float) const {
+    y[(int64_t)n * ld + o] = __float2half_rn(v);
+  }
+};
+
+// Query up-projection: rows [0, n_h*d_hc) of [W^UQ; W^QR] are q^C, the rest q^R with RoPE.
+template <typename T>
+struct EpQuery {
+  T* q_c;
+  T* q_r;
+  int64_t qc_tok, qc_head, qr_tok, qr_head;
+  const int32_t* pos;
+  int n_h, d_hc, d_hr;
+  float base;
+  __device__ void operator()(int o, int n, float v, float vp) const {
+    const int nc = n_h * d_hc;
+    if (o < nc) {
+      q_c[n * qc_tok + (o / d_hc) * qc_head + (o % d_hc)] = from_f<T>(v);
+    } else {
+      const int r = o - nc, i = r / d_hr, e = r % d_hr;
+      float c, s;
+      rope_cs(pos[n], e >> 1, d_hr, base, &c, &s);
+      v = (e & 1) ? (vp * s + v * c) : (v * c - vp * s);
+      q_r[n * qr_tok + i * qr_head + e] = from_f<T>(v);
+    }
+  }
+};
+
+bool tmap_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld_elems,
+               int box_rows) {
+  const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)ld_elems * 2};
+  const uint32_t box[2] = {64, (uint32_t)box_rows};
+  return make_tmap(m, base, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+
+template <int BN, class Ep>
+mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
+  CUtensorMap tw0, tw1, tx, tx2;
+  const int m0 = a.O0 / 128;
+  if (!tmap_rows(&tw0, a.W0, a.O0, a.K, a.K, 128)) return MLA_ERR_CUDA;
+  if (!tmap_rows(&tw1, a.W1 ? a.W1 : a.W0, a.W1 ? a.O1 : a.O0, a.K, a.K, 128)) return MLA_ERR_CUDA;
+  if (!tmap_rows(&tx, a.X, a.N, a.K, a.ldx, BN)) return MLA_ERR_CUDA;
+  if (!tmap_rows(&tx2, a.X2 ? a.X2 : a.X, a.N, a.K, a.ldx, BN)) return MLA_ERR_CUDA;
+  const int m_tiles = m0 + (a.W1 ? ceil_div(a.O1, 128) : 0);
+  const uint32_t smem = ProjSmem<BN>::kBytes + 1024;
+  auto kern = proj_gemm_kernel<BN, Ep>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  dim3 grid(m_tiles, ceil_div(a.N, BN));
+  TraceScope ts(a.kid, st);
+  kern<<<grid, kThreads, smem, st>>>(tw0, tw1, tx, tx2, m0, a.O0 + (a.W1 ? a.O1 : 0), a.N,
+                                     a.K / 64, a.X2 ? 1 : 0, ep);
+  return launch_status();
+}
+
+template <class Ep>
+mla_status_t launch_proj(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
+  if (a.N <= 0) return MLA_OK;
+  if (a.K % 64 || a.O0 % 128) return MLA_ERR_UNSUPPORTED;
+  if (a.N <= 32) return launch_proj_bn<32>(a, ep, st);
+  if (a.N <= 64) return launch_proj_bn<64>(a, ep, st);
+  if (a.N <= 128) return launch_proj_bn<128>(a, ep, st);
+  return launch_proj_bn<256>(a, ep, st);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------- entry points
+mla_status_t tc_append(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                       const int32_t* seq_idx, const int32_t* pos, int n, mla_cache_t* cache,
+                       void* packed, int kid, cudaStream_t st) {
+  ProjArgs a{};
+  a.W0 = w->W_DKV;
+  a.O0 = d->d_c;
+  a.W1 = w->W_KR;
+  a.O1 = d->d_hr;
+  a.K = d->d;
+  a.X = h;
+  a.ldx = d->d;
+  a.N = n;
+  a.kid = kid;
+  EpAppend ep{(__nv_bfloat16*)cache->rows, (int64_t)(d->d_c + d->d_hr), cache->capacity,
+              cache->seq_base, seq_idx, pos, (__nv_bfloat16*)packed, d->d_c, d->d_hr,
+              d->rope_base};
+  return launch_proj(a, ep, st);
+}
+
+mla_status_t tc_q_down(const mla_dims_t* d, const mla_weights_t* w, const void* h, int n,
+                       void* cq_hi, void* cq_lo, int kid, cudaStream_t st) {
+  ProjArgs a{};
+  a.W0 = w->W_DQ;
+  a.O0 = d->d_cq;
+  a.K = d->d;
+  a.X = h;
+  a.ldx = d->d;
+  a.N = n;
+  a.kid = kid;
+  EpStoreBF16 ep{(__nv_bfloat16*)cq_hi, (__nv_bfloat16*)cq_lo, d->d_cq};
+  return launch_proj(a, ep, st);
+}
+
+mla_status_t tc_q_up(const mla_dims_t* d, const mla_weights_t* w, const void* cq_hi,
+                     const void* cq_lo, const int32_t* pos, int n, void* q_c, void* q_r,
+                     int64_t qc_tok, int64_t qc_head, int64_t qr_tok, int64_t qr_head,
+                     bool f16_out, int kid, cudaStream_t st) {
+  ProjArgs a{};
+  a.W0 = w->W_UQ;
+  a.O0 = d->n_h * d->d_hc;
+  a.W1 = w->W_QR;
+  a.O1 = d->n_h * d->d_hr;
+  a.K = d->d_cq;
+  a.X = cq_hi;
+  a.X2 = cq_lo;
+  a.ldx = d->d_cq;
+  a.N = n;
+  a.kid = kid;
+  if (f16_out) {
+    EpQuery<__half> ep{(__half*)q_c, (__half*)q_r, qc_tok, qc_head, qr_tok, qr_head, pos,
+                       d->n_h, d->d_hc, d->d_hr, d->rope_base};
+    return launch_proj(a, ep, st);
+  }
+  EpQuery<__nv_bfloat16> ep{(__nv_bfloat16*)q_c, (__nv_bfloat16*)q_r, qc_tok, qc_head, qr_tok,
+                            qr_head, pos, d->n_h, d->d_hc, d->d_hr, d->rope_base};
+  return launch_proj(a, ep, st);
+}
+
+mla_status_t tc_expand(const void* W, int O, const void* latent, int64_t ld_latent, int K, int n,
+                       void* y, int kid, cudaStream_t st) {
+  ProjArgs a{};
+  a.W0 = W;
+  a.O0 = O;
+  a.K = K;
+  a.X = latent;
+  a.ldx = ld_latent;
+  a.N = n;
+  a.kid = kid;
+  EpStoreF16 ep{(__half*)y, O};
+  return launch_proj(a, ep, st);
+}
+
+}  // namespace mla

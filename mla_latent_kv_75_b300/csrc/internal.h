@@ -45,4 +45,18 @@ mla_status_t simt_prefill(const mla_dims_t* d, const mla_weights_t* w, const voi
                           const int32_t* cu, int B, int n, int max_T, mla_cache_t* cache,
                           void* ws, float* o, cudaStream_t st);
 
+// Tensor-core kernels (V2 widths, bf16): gemm_tc.cu
+bool fast_dims(const mla_dims_t* d);
+mla_status_t tc_append(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                       const int32_t* seq_idx, const int32_t* pos, int n, mla_cache_t* cache,
+                       void* packed, int kid, cudaStream_t st);
+mla_status_t tc_q_down(const mla_dims_t* d, const mla_weights_t* w, const void* h, int n,
+                       void* cq_hi, void* cq_lo, int kid, cudaStream_t st);
+mla_status_t tc_q_up(const mla_dims_t* d, const mla_weights_t* w, const void* cq_hi,
+                     const void* cq_lo, const int32_t* pos, int n, void* q_c, void* q_r,
+                     int64_t qc_tok, int64_t qc_head, int64_t qr_tok, int64_t qr_head,
+                     bool f16_out, int kid, cudaStream_t st);
+mla_status_t tc_expand(const void* W, int O, const void* latent, int64_t ld_latent, int K, int n,
+                       void* y, int kid, cudaStream_t st);
+
 }  // namespace mla
