@@ -51,8 +51,12 @@ def decode_kernel_costs(wl: mi.Workload):
                        flops=2 * B * d.n_h * d.d_hc * d.d_c),
         "decode_attn": dict(bytes=rows * d.row * e + B * d.n_h * (d.d_c + d.d_hr) * e,
                             flops=rows * (2 * d.n_h * d.row + 2 * d.n_h * d.d_c)),
+        # SIMT path: merge + W^UV in one kernel; tensor-core path: merge, then unabsorb
         "decode_combine": dict(bytes=nc * d.d_c * e + B * d.n_h * d.d_hc * 4,
                                flops=2 * B * d.n_h * d.d_hc * d.d_c),
+        "decode_merge": dict(bytes=0, flops=0),
+        "unabsorb": dict(bytes=nc * d.d_c * e + B * d.n_h * d.d_hc * 4,
+                         flops=2 * B * d.n_h * d.d_hc * d.d_c),
     }
     return out
 
@@ -331,7 +335,7 @@ def run_ours(args, rank, world, local_rank):
         c = costs.get(name)
         entry = {"launches": len(ts), "avg_us": round(avg_ms * 1e3, 3),
                  "share": round(sum(ts) / sum(sum(v) for v in per.values()), 4)}
-        if c:
+        if c and c["bytes"] > 0:
             gbs = c["bytes"] / (avg_ms * 1e-3) / 1e9
             tfl = c["flops"] / (avg_ms * 1e-3) / 1e12
             floor_s = max(c["bytes"] / (peaks["hbm_gbs"] * 1e9),
@@ -361,10 +365,10 @@ def run_ours(args, rank, world, local_rank):
         roofline["traffic"] = None
 
     # the absorbed-decode call alone (absorb + attention + combine)
-    dec_names = ("absorb", "decode_attn", "decode_combine")
+    dec_names = ("absorb", "decode_attn", "decode_combine", "decode_merge", "unabsorb")
     dec_s = sum(statistics.mean(per[n]) for n in dec_names if n in per) * 1e-3
-    dec_bytes = sum(costs[n]["bytes"] for n in dec_names)
-    dec_flops = sum(costs[n]["flops"] for n in dec_names)
+    dec_bytes = sum(costs[n]["bytes"] for n in dec_names if n in per)
+    dec_flops = sum(costs[n]["flops"] for n in dec_names if n in per)
     decode_call = None
     if dec_s > 0:
         floor_s = max(dec_bytes / (peaks["hbm_gbs"] * 1e9), dec_flops / (peaks["bf16_tflops"] * 1e12))

@@ -61,7 +61,8 @@ struct TraceState {
 TraceState g_trace;
 const char* const kKernelNames[K_NUM_IDS] = {
     "append", "q_down", "q_up", "absorb", "decode_attn", "decode_combine", "token_map",
-    "prefill_append", "prefill_q_down", "prefill_q_up", "expand_k", "expand_v", "prefill_attn"};
+    "prefill_append", "prefill_q_down", "prefill_q_up", "expand_k", "expand_v", "prefill_attn",
+    "decode_merge", "unabsorb"};
 }  // namespace
 
 void trace_before(int kernel_id, cudaStream_t st) {
@@ -159,7 +160,7 @@ mla_status_t mla_decode_workspace_size(const mla_dims_t* d, int32_t B, int32_t m
                                        size_t* bytes) {
   MLA_TRY(check_dims(d));
   if (!bytes || B < 0 || max_len < 0) return MLA_ERR_INVALID_ARG;
-  *bytes = simt_decode_ws(d, B, max_len);
+  *bytes = fast_dims(d) ? tc_decode_ws(d, B) : simt_decode_ws(d, B, max_len);
   return MLA_OK;
 }
 
@@ -181,6 +182,8 @@ mla_status_t mla_decode_absorbed(const mla_dims_t* d, const mla_weights_t* w, co
   MLA_TRY(mla_decode_workspace_size(d, B, max_len, &need));
   if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
   MLA_TRY(check_ptr(ws));
+  if (fast_dims(d))
+    return tc_decode(d, w, q_c, q_r, cache, seq_len, B, max_len, ws, o, as_stream(stream));
   return simt_decode(d, w, q_c, q_r, cache, seq_len, B, max_len, ws, o, as_stream(stream));
 }
 

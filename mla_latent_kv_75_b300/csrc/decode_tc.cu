@@ -1,0 +1,690 @@
+// Weight-absorbed decode on the tensor cores for the DeepSeek-V2 widths (n_h 128, d_h^C 128,
+// d_h^R 64, d_c 512, bf16): "从LLaMA到DeepSeek[01] - MLA（上）" §六 (absorption by
+// associativity) and "MLA前向计算流程" §三分支计算 ④ (softmax over j = 1..t, scale
+// 1/sqrt(d_h^C + d_h^R)).
+//
+// Four launches:
+//   absorb      q~[b,i,:] = (W^UK_i)^T q^C[b,i,:]        grouped tcgen05 GEMM (gemm_tc.cu)
+//   attention   split-KV latent attention, this file     (m, l, O~) partials per segment
+//   merge       log-sum-exp merge of the partials        o~[b,i,:] as a hi/lo bf16 pair
+//   unabsorb    o[b,i,:] = W^UV_i o~[b,i,:]              grouped tcgen05 GEMM (gemm_tc.cu)
+//
+// The attention kernel runs one cluster of two CTAs per pair of SMs. All 128 heads form the M
+// dimension of every MMA. The pair splits the 576-wide cache row: CTA 0 owns latent columns
+// [0, 256) plus the 64 RoPE columns, CTA 1 owns latent columns [256, 512). Each CTA
+//   - streams only its columns of each 64-row cache tile into shared memory with TMA,
+//   - computes its partial score S_r = Q_r K_r^T (K = 320 or 256; Q_r lives in TMEM),
+//   - sends S_r to the peer through distributed shared memory (st.async) and adds the peer's
+//     partial, so both CTAs hold the same full score tile,
+//   - runs the same online softmax (exp2, lazy rescaling) on it, writes P (bf16) to shared
+//     memory, and accumulates O_r += P V_r into TMEM, where V_r is the same shared-memory
+//     tile read as an MN-major operand (O_r is 128 heads x 256 latent columns, fp32).
+// No cache byte is read twice and no MMA work is duplicated across the pair.
+//
+// Work split: the cache tiles of all sequences form one list (sequence by sequence); pair p of
+// P takes the contiguous range [p*T/P, (p+1)*T/P). Every (sequence b, pair p) intersection is
+// one segment whose partial result goes to slot b + p, which is unique because both ranges are
+// ordered; the merge kernel recomputes the same ranges to find a sequence's slots.
+#include <mutex>
+
+#include "internal.h"
+#include "proj_tc.h"
+#include "tc.cuh"
+
+namespace mla {
+
+using namespace tc;
+
+namespace {
+
+constexpr int kDC = 512;          // d_c
+constexpr int kRowElems = 576;    // d_c + d_h^R
+constexpr int kHeads = 128;       // n_h
+constexpr int kTile = 64;         // cache rows per tile
+constexpr int kStages = 4;
+constexpr int kBox = 64 * 64 * 2;  // one TMA box: 64 columns x 64 rows of bf16 (8 KB)
+constexpr int kStageBytes = 5 * kBox;
+constexpr int kPBytes = kHeads * kTile * 2;  // P tile, bf16
+constexpr int kXBytes = kHeads * kTile * 4;  // partial-score exchange tile, fp32
+constexpr int kOffP = kStages * kStageBytes;
+constexpr int kOffX = kOffP + 2 * kPBytes;
+constexpr int kOffBar = kOffX + kXBytes;
+constexpr int kThreads = 192;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;
+constexpr int kMaxPairs = 80;  // partial slots are sized for at most this many SM pairs
+
+// tensor-memory columns
+constexpr uint32_t kColO = 0;    // O_r: 256 fp32 columns
+constexpr uint32_t kColS = 256;  // S tile: 64 fp32 columns
+constexpr uint32_t kColQ = 320;  // Q_r: 160 (rank 0) or 128 (rank 1) columns of bf16 pairs
+
+constexpr float kTau = 8.f;  // lazy rescale threshold (log2 units): p <= 2^8 between rescales
+
+struct Shared {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t s_full, s_free, p_full[2], pv_done, x_full, x_empty, q_full;
+  uint32_t tmem_slot;
+  int abort;
+  int b0, j0;
+  long long t_begin, t_end;
+  long long red[8];
+};
+static_assert(sizeof(Shared) <= 256, "barrier block");
+
+struct SeqInfo {
+  int L, n;
+  int64_t base;
+};
+
+// Length, tile count and first row of sequence b, with the same clamping as the other decode
+// kernels: lengths above max_len are cut to max_len; a sequence whose rows leave the cache is
+// treated as empty. `flag` latches the matching status.
+__device__ __forceinline__ SeqInfo seq_info(const int32_t* __restrict__ seq_len,
+                                            const int64_t* __restrict__ seq_base, int b,
+                                            int max_len, int64_t capacity, bool flag) {
+  int L = seq_len[b];
+  const int64_t base = seq_base[b];
+  if (L < 0 || L > max_len) {
+    if (flag) flag_status(MLA_ERR_LENGTH);
+    L = L < 0 ? 0 : max_len;
+  }
+  if (L > 0 && (base < 0 || base + L > capacity)) {
+    if (flag) flag_status(MLA_ERR_CAPACITY);
+    L = 0;
+  }
+  return {L, (L + kTile - 1) / kTile, base};
+}
+
+template <int NT>
+__device__ __forceinline__ long long block_sum(long long v, long long* red) {
+  for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  long long s = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) s += red[w];
+  return s;
+}
+
+template <int NT>
+__device__ __forceinline__ long long block_excl_scan(long long v, long long* red,
+                                                     long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
+  long long before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    if (w < warp) before += red[w];
+    tot += red[w];
+  }
+  *total = tot;
+  return before + x - v;
+}
+
+__device__ __forceinline__ long long pair_start(int p, long long T, int P) {
+  return (long long)p * T / P;
+}
+
+// Pair whose tile range contains tile t.
+__device__ __forceinline__ int pair_of(long long t, long long T, int P) {
+  int p = (int)(t * P / T);
+  if (p >= P) p = P - 1;
+  while (p + 1 < P && pair_start(p + 1, T, P) <= t) ++p;
+  while (p > 0 && pair_start(p, T, P) > t) --p;
+  return p;
+}
+
+// Walks the tiles of one pair's range sequence by sequence.
+struct Cursor {
+  int b, j;
+  SeqInfo s;
+  __device__ void next(const int32_t* seq_len, const int64_t* seq_base, int max_len,
+                       int64_t capacity) {
+    if (++j < s.n) return;
+    j = 0;
+    do {
+      ++b;
+      s = seq_info(seq_len, seq_base, b, max_len, capacity, false);
+    } while (s.n == 0);
+  }
+};
+
+// Warp-uniform bounded wait used by the softmax warps (every lane polls; the warp leaves
+// together, either when all lanes saw the phase complete or on timeout / abort).
+template <bool kCluster>
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  uint64_t t0 = 0;
+  for (int it = 0;; ++it) {
+    const bool ok = kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((it & 63) == 63) {
+      int stop = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (t0 == 0) t0 = global_ns();
+        if (*abort) {
+          stop = 1;
+        } else if (global_ns() - t0 > kWaitLimitNs) {
+          flag_status(MLA_ERR_TIMEOUT);
+          *abort = 1;
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------------------------------------
+// The attention kernel
+// ------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_rows,
+                          const __nv_bfloat16* __restrict__ qt,   // [B, 128, 512]
+                          const __nv_bfloat16* __restrict__ q_r,  // [B, 128, 64]
+                          const int32_t* __restrict__ seq_len,
+                          const int64_t* __restrict__ seq_base, int64_t capacity, int B,
+                          int max_len, float scale_log2, float* __restrict__ part_o,
+                          float* __restrict__ part_ml) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Shared& sh = *reinterpret_cast<Shared*>(smem + kOffBar);
+  volatile int* abort = &sh.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int P = gridDim.x / 2, p = blockIdx.x / 2;
+  const int nbox = rank == 0 ? 5 : 4;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], 1);
+    }
+    mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.s_free, 4);
+    mbar_init(&sh.p_full[0], 4);
+    mbar_init(&sh.p_full[1], 4);
+    mbar_init(&sh.pv_done, 1);
+    mbar_init(&sh.x_full, 1);
+    mbar_init(&sh.x_empty, 4);
+    mbar_init(&sh.q_full, 4);
+    sh.abort = 0;
+    sh.b0 = 0;
+    sh.j0 = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) tma_prefetch(&tm_rows);
+
+  // ---- plan: total tile count T, this pair's range and its first (sequence, tile)
+  long long local = 0;
+  for (int b = threadIdx.x; b < B; b += kThreads)
+    local += seq_info(seq_len, seq_base, b, max_len, capacity, blockIdx.x == 0).n;
+  const long long T = block_sum<kThreads>(local, sh.red);
+  const long long t_begin = T > 0 ? pair_start(p, T, P) : 0;
+  const long long t_end = T > 0 ? pair_start(p + 1, T, P) : 0;
+  if (t_begin < t_end) {
+    long long carry = 0;
+    for (int b_lo = 0; b_lo < B; b_lo += kThreads) {
+      const int b = b_lo + threadIdx.x;
+      const int n = b < B ? seq_info(seq_len, seq_base, b, max_len, capacity, false).n : 0;
+      long long tot;
+      const long long excl = carry + block_excl_scan<kThreads>(n, sh.red, &tot);
+      if (n > 0 && excl <= t_begin && t_begin < excl + n) {
+        sh.b0 = b;
+        sh.j0 = (int)(t_begin - excl);
+      }
+      carry += tot;
+      if (carry > t_begin) break;
+    }
+  }
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before any remote arrive / st.async
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_slot;
+  const int nt = (int)(t_end - t_begin);
+
+  if (nt > 0 && warp == 0 && lane == 0) {
+    // ------------------------------------------------------------- TMA producer
+    Cursor cur{sh.b0, sh.j0, seq_info(seq_len, seq_base, sh.b0, max_len, capacity, false)};
+    int issued = 0;
+    for (int t = 0; t < nt; ++t) {
+      const int s = t % kStages, r = t / kStages;
+      if (r > 0 && !mbar_wait(&sh.empty[s], (r - 1) & 1, abort)) break;
+      uint8_t* stage = smem + s * kStageBytes;
+      mbar_arrive_expect_tx(&sh.full[s], nbox * kBox);
+      const int y = (int)(cur.s.base + (int64_t)cur.j * kTile);
+      for (int k = 0; k < nbox; ++k) {
+        const int x = rank == 0 ? (k < 4 ? k * 64 : kDC) : 256 + k * 64;
+        tma_load_2d(stage + k * kBox, &tm_rows, &sh.full[s], x, y);
+      }
+      ++issued;
+      if (t + 1 < nt) cur.next(seq_len, seq_base, max_len, capacity);
+    }
+    for (int t = (issued > kStages ? issued - kStages : 0); t < issued; ++t)
+      mbar_wait(&sh.full[t % kStages], (t / kStages) & 1, abort);
+  } else if (nt > 0 && warp == 1 && lane == 0) {
+    // ------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc_s = idesc_f16(128, 64, 1, 0, 0);
+    constexpr uint32_t idesc_o = idesc_f16(128, 256, 1, 0, 1);
+    const int nks = rank == 0 ? 20 : 16;  // 16-wide K steps of the score MMA
+    Cursor cur{sh.b0, sh.j0, seq_info(seq_len, seq_base, sh.b0, max_len, capacity, false)};
+    int seg = 0;
+    bool ok = true;
+    auto issue_s = [&](int t) -> bool {
+      const int s = t % kStages;
+      if (!mbar_wait(&sh.full[s], (t / kStages) & 1, abort)) return false;
+      tc_fence_after();
+      const uint32_t st = smem_u32(smem + s * kStageBytes);
+      for (int ks = 0; ks < nks; ++ks)
+        mma_ts(tmem + kColS, tmem + kColQ + ks * 8,
+               smem_desc(st + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024), idesc_s, ks > 0);
+      mma_commit(&sh.s_full);
+      return true;
+    };
+    ok = mbar_wait(&sh.q_full, 0, abort) && (tc_fence_after(), issue_s(0));
+    for (int t = 0; ok && t < nt; ++t) {
+      const bool last_in_seg = cur.j + 1 == cur.s.n;
+      const bool seg_first = t == 0 || cur.j == 0;  // O starts from zero
+      if (t + 1 < nt && !last_in_seg) {
+        if (!mbar_wait(&sh.s_free, t & 1, abort) || !issue_s(t + 1)) break;
+      }
+      if (!mbar_wait(&sh.p_full[t & 1], (t >> 1) & 1, abort)) break;
+      tc_fence_after();
+      const uint32_t st = smem_u32(smem + (t % kStages) * kStageBytes);
+      const uint32_t pb = smem_u32(smem + kOffP + (t & 1) * kPBytes);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(tmem + kColO, smem_desc(pb + ks * 32, 16, 1024),
+               smem_desc(st + ks * 2048, 8192, 1024), idesc_o, (!seg_first || ks > 0) ? 1u : 0u);
+      mma_commit(&sh.empty[t % kStages]);
+      mma_commit(&sh.pv_done);
+      if (t + 1 < nt && last_in_seg) {
+        ++seg;
+        if (!mbar_wait(&sh.q_full, seg & 1, abort) || !mbar_wait(&sh.s_free, t & 1, abort))
+          break;
+        tc_fence_after();
+        if (!issue_s(t + 1)) break;
+      }
+      if (t + 1 < nt) cur.next(seq_len, seq_base, max_len, capacity);
+    }
+  } else if (nt > 0 && warp >= 2) {
+    // ------------------------------------------------------------- softmax warps
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int h = q * 32 + lane;            // head = TMEM lane
+    const int ts = threadIdx.x - 64;        // 0..127 among the softmax threads
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    uint8_t* X = smem + kOffX;
+    const uint32_t peer = rank ^ 1u;
+    const uint32_t peer_x = mapa_shared(smem_u32(X), peer) + h * 256;
+    const uint32_t peer_xfull = mapa_shared(smem_u32(&sh.x_full), peer);
+    const uint32_t peer_xempty = mapa_shared(smem_u32(&sh.x_empty), peer);
+    const int sw = h & 7;
+
+    // Q_r of sequence b into TMEM (two bf16 per column)
+    auto load_q = [&](int b) {
+      const uint4* src = reinterpret_cast<const uint4*>(qt + ((int64_t)b * kHeads + h) * kDC +
+                                                        rank * 256);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {  // 4 x 32 columns = 256 bf16
+        uint32_t r[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = src[c * 8 + k];
+          r[4 * k] = v.x;
+          r[4 * k + 1] = v.y;
+          r[4 * k + 2] = v.z;
+          r[4 * k + 3] = v.w;
+        }
+        tmem_st32u(lane_base + kColQ + c * 32, r);
+      }
+      if (rank == 0) {  // q^R: 64 bf16 = 32 columns
+        const uint4* sr = reinterpret_cast<const uint4*>(q_r + ((int64_t)b * kHeads + h) * 64);
+        uint32_t r[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = sr[k];
+          r[4 * k] = v.x;
+          r[4 * k + 1] = v.y;
+          r[4 * k + 2] = v.z;
+          r[4 * k + 3] = v.w;
+        }
+        tmem_st32u(lane_base + kColQ + 128, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.q_full);
+    };
+
+    Cursor cur{sh.b0, sh.j0, seq_info(seq_len, seq_base, sh.b0, max_len, capacity, false)};
+    load_q(cur.b);
+    float m_used = -INFINITY, l_sum = 0.f;
+    for (int t = 0; t < nt; ++t) {
+      const int j = cur.j;
+      const int valid = min(kTile, cur.s.L - j * kTile);
+      float s[64];
+      if (!warp_wait<false>(&sh.s_full, t & 1, abort)) break;
+      tc_fence_after();
+      tmem_ld32(lane_base + kColS, *reinterpret_cast<float(*)[32]>(&s[0]));
+      tmem_ld32(lane_base + kColS + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.s_free);
+
+      // exchange partial scores with the peer CTA
+      if (t > 0 && !warp_wait<true>(&sh.x_empty, (t - 1) & 1, abort)) break;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_async_v4(peer_x + ((c ^ sw) << 4), peer_xfull, s[4 * c], s[4 * c + 1], s[4 * c + 2],
+                    s[4 * c + 3]);
+      if (ts == 0) mbar_arrive_expect_tx(&sh.x_full, kXBytes);
+      if (!warp_wait<true>(&sh.x_full, t & 1, abort)) break;
+      const uint8_t* xrow = X + h * 256;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float4 v = *reinterpret_cast<const float4*>(xrow + ((c ^ sw) << 4));
+        s[4 * c] += v.x;
+        s[4 * c + 1] += v.y;
+        s[4 * c + 2] += v.z;
+        s[4 * c + 3] += v.w;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(peer_xempty);
+
+      // online softmax in log2 units with lazy rescaling
+      float mt = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        s[i] = i < valid ? s[i] * scale_log2 : -INFINITY;
+        mt = fmaxf(mt, s[i]);
+      }
+      const bool first = t == 0 || j == 0;  // first tile of a segment
+      const float m_new = first ? mt : (mt > m_used + kTau ? mt : m_used);
+      const float alpha = first ? 0.f : exp2f(m_used - m_new);
+      if (__any_sync(0xffffffffu, !first && m_new != m_used)) {
+        if (!warp_wait<false>(&sh.pv_done, (t - 1) & 1, abort)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          float o[32];
+          tmem_ld32(lane_base + kColO + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] *= alpha;
+          tmem_st32(lane_base + kColO + c * 32, o);
+        }
+        tmem_wait_st();
+      }
+      l_sum *= alpha;
+      m_used = m_new;
+
+      // P (bf16) -> shared memory, K-major with the 128-byte swizzle
+      uint8_t* prow = smem + kOffP + (t & 1) * kPBytes + h * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float p0 = exp2f(s[8 * c + 2 * k] - m_used);
+          const float p1 = exp2f(s[8 * c + 2 * k + 1] - m_used);
+          w[k] = pack_bf16(p0, p1);
+          const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+          l_sum += __low2float(pb) + __high2float(pb);
+        }
+        *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      if (valid < kTile) {
+        // rows past the sequence end may hold anything (even NaN): zero them in the V operand
+        uint8_t* stage = smem + (t % kStages) * kStageBytes;
+        const int n16 = (kTile - valid) * 8;  // 16-byte chunks per box
+        for (int e = ts; e < 4 * n16; e += 128) {
+          const int box = e / n16, r = e % n16;
+          *reinterpret_cast<uint4*>(stage + box * kBox + valid * 128 + r * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.p_full[t & 1]);
+
+      if (j + 1 == cur.s.n || t + 1 == nt) {
+        // end of a segment (end of the sequence or of this pair's range): the next
+        // sequence's Q first, then O_r and (m, l) to the segment's partial slot
+        const int b_done = cur.b;
+        if (t + 1 < nt) {
+          cur.next(seq_len, seq_base, max_len, capacity);
+          load_q(cur.b);
+        }
+        if (!warp_wait<false>(&sh.pv_done, t & 1, abort)) break;
+        tc_fence_after();
+        const int64_t slot = (int64_t)b_done + p;
+        float* dst = part_o + (slot * kDC + rank * 256) * kHeads + h;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          float o[32];
+          tmem_ld32(lane_base + kColO + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) dst[(int64_t)(c * 32 + k) * kHeads] = o[k];
+        }
+        if (rank == 0) {
+          part_ml[slot * 256 + h] = m_used;
+          part_ml[slot * 256 + 128 + h] = l_sum;
+        }
+        tc_fence_before();
+        m_used = -INFINITY;
+        l_sum = 0.f;
+      } else if (t + 1 < nt) {
+        cur.next(seq_len, seq_base, max_len, capacity);
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  cluster_sync();  // no CTA leaves while the peer may still address its shared memory
+}
+
+// ------------------------------------------------------------------------------------------
+// Merge of the partials of one sequence: o~ = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,
+// stored as a hi/lo pair of bf16 (o~ = hi + lo to about 2^-16 relative).
+// grid (B, 8): blockIdx.y picks 64 latent columns; thread = (head, half of those columns).
+// ------------------------------------------------------------------------------------------
+constexpr int kMergeThreads = 256;
+
+__global__ void __launch_bounds__(kMergeThreads)
+    decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                        const int32_t* __restrict__ seq_len, const int64_t* __restrict__ seq_base,
+                        int64_t capacity, int B, int max_len, int P,
+                        __nv_bfloat16* __restrict__ ol_hi, __nv_bfloat16* __restrict__ ol_lo) {
+  __shared__ long long red[8];
+  const int b = blockIdx.x;
+  const int h = threadIdx.x & 127;
+  const int c0 = blockIdx.y * 64 + (threadIdx.x >> 7) * 32;
+  long long tot_local = 0, before_local = 0;
+  for (int k = threadIdx.x; k < B; k += kMergeThreads) {
+    const int n = seq_info(seq_len, seq_base, k, max_len, capacity, false).n;
+    tot_local += n;
+    if (k < b) before_local += n;
+  }
+  const long long T = block_sum<kMergeThreads>(tot_local, red);
+  const long long cum = block_sum<kMergeThreads>(before_local, red);
+  const int n = seq_info(seq_len, seq_base, b, max_len, capacity, false).n;
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+  float inv_l = 0.f;
+  if (n > 0) {
+    const int p_first = pair_of(cum, T, P), p_last = pair_of(cum + n - 1, T, P);
+    float M = -INFINITY;
+    // pairs with an empty range (fewer tiles than pairs) wrote nothing
+    for (int pp = p_first; pp <= p_last; ++pp)
+      if (pair_start(pp, T, P) < pair_start(pp + 1, T, P))
+        M = fmaxf(M, part_ml[((int64_t)b + pp) * 256 + h]);
+    float lsum = 0.f;
+    for (int pp = p_first; pp <= p_last; ++pp) {
+      if (pair_start(pp, T, P) == pair_start(pp + 1, T, P)) continue;
+      const int64_t slot = (int64_t)b + pp;
+      const float w = exp2f(part_ml[slot * 256 + h] - M);
+      lsum += w * part_ml[slot * 256 + 128 + h];
+      const float* src = part_o + (slot * kDC + c0) * kHeads + h;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = fmaf(w, src[(int64_t)i * kHeads], acc[i]);
+    }
+    inv_l = lsum > 0.f ? 1.f / lsum : 0.f;
+  }
+  const int64_t o = ((int64_t)b * kHeads + h) * kDC + c0;
+#pragma unroll
+  for (int i = 0; i < 32; i += 8) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float v0 = acc[i + 2 * k] * inv_l, v1 = acc[i + 2 * k + 1] * inv_l;
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(v0, v1);
+      const __nv_bfloat162 lo =
+          __floats2bfloat162_rn(v0 - __low2float(hi), v1 - __high2float(hi));
+      hw[k] = *reinterpret_cast<const uint32_t*>(&hi);
+      lw[k] = *reinterpret_cast<const uint32_t*>(&lo);
+    }
+    *reinterpret_cast<uint4*>(ol_hi + o + i) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(ol_lo + o + i) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------------------
+struct Layout {
+  size_t off_qt, off_hi, off_lo, off_part, off_ml, total;
+};
+
+Layout layout(int B) {
+  Layout L;
+  const size_t slots = (size_t)B + kMaxPairs;
+  L.off_qt = 0;
+  L.off_hi = align_up(L.off_qt + (size_t)B * kHeads * kDC * 2, 256);
+  L.off_lo = align_up(L.off_hi + (size_t)B * kHeads * kDC * 2, 256);
+  L.off_part = align_up(L.off_lo + (size_t)B * kHeads * kDC * 2, 256);
+  L.off_ml = align_up(L.off_part + slots * kDC * kHeads * 4, 256);
+  L.total = align_up(L.off_ml + slots * 256 * 4, 256);
+  return L;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_pairs[kMaxDevices] = {};
+
+cudaLaunchConfig_t attn_config(int pairs, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Number of CTA pairs that are resident at once on the current device (one pair per two SMs
+// that can host a 2-CTA cluster), capped at kMaxPairs. Set up once per device.
+mla_status_t attn_pairs(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_pairs[dev]) {
+    if (cudaFuncSetAttribute(decode_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = attn_config(kMaxPairs, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_attn_tc_kernel, &cfg) != cudaSuccess || n < 1)
+      return MLA_ERR_CUDA;
+    g_pairs[dev] = n < kMaxPairs ? n : kMaxPairs;
+  }
+  *out = g_pairs[dev];
+  return MLA_OK;
+}
+
+}  // namespace
+
+size_t tc_decode_ws(const mla_dims_t*, int B) { return layout(B).total; }
+
+mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* q_c,
+                       const void* q_r, const mla_cache_t* cache, const int32_t* seq_len, int B,
+                       int max_len, void* ws, float* o, cudaStream_t st) {
+  const Layout L = layout(B);
+  char* wsb = (char*)ws;
+  __nv_bfloat16* qt = (__nv_bfloat16*)(wsb + L.off_qt);
+  __nv_bfloat16* hi = (__nv_bfloat16*)(wsb + L.off_hi);
+  __nv_bfloat16* lo = (__nv_bfloat16*)(wsb + L.off_lo);
+  float* part = (float*)(wsb + L.off_part);
+  float* ml = (float*)(wsb + L.off_ml);
+  int pairs = 0;
+  mla_status_t s = attn_pairs(&pairs);
+  if (s != MLA_OK) return s;
+
+  // 1. q~ = (W^UK_i)^T q^C_i
+  s = tc_absorb(d, w, q_c, B, qt, K_ABSORB, st);
+  if (s != MLA_OK) return s;
+
+  // 2. attention over the latent cache
+  if (max_len > 0 && cache->capacity > 0) {
+    CUtensorMap tm;
+    const uint64_t dims[2] = {(uint64_t)kRowElems, (uint64_t)cache->capacity};
+    const uint64_t strides[1] = {(uint64_t)kRowElems * 2};
+    const uint32_t box[2] = {64, (uint32_t)kTile};
+    if (!make_tmap(&tm, cache->rows, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+      return MLA_ERR_CUDA;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = attn_config(pairs, st, attr);
+    const float scale_log2 = softmax_scale(d) * 1.4426950408889634f;
+    TraceScope ts(K_DECODE_ATTN, st);
+    if (cudaLaunchKernelEx(&cfg, decode_attn_tc_kernel, tm, (const __nv_bfloat16*)qt,
+                           (const __nv_bfloat16*)q_r, seq_len, cache->seq_base, cache->capacity,
+                           B, max_len, scale_log2, part, ml) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+
+  // 3. merge the partials of each sequence (o~ = 0 for empty sequences)
+  {
+    TraceScope ts(K_DECODE_MERGE, st);
+    decode_merge_kernel<<<dim3(B, kDC / 64), kMergeThreads, 0, st>>>(
+        part, ml, seq_len, cache->seq_base, max_len > 0 ? cache->capacity : 0, B, max_len,
+        pairs, hi, lo);
+    s = launch_status();
+    if (s != MLA_OK) return s;
+  }
+
+  // 4. o = W^UV_i o~
+  return tc_unabsorb(d, w, hi, lo, B, o, K_UNABSORB, st);
+}
+
+}  // namespace mla

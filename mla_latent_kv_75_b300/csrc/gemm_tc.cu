@@ -27,13 +27,21 @@ struct ProjSmem {
   static constexpr uint32_t kBytes = kBars + 256;
 };
 
-template <int BN, class Ep>
+// Operand modes of the projection GEMM.
+//   kPlain:     A = [W0; W1] rows (K-major), B = X rows [N, K] (K-major).
+//   kGroupedK:  grouped per head: m-tile i belongs to group g = i / mt_group; A rows as in
+//               kPlain, B = X[n, g, :] read through a 3-D tensor map (K, groups, N).
+//   kGroupedMN: as kGroupedK but A = W^T: A[m, k] = W0[g * K + k, (i % mt_group) * 128 + m],
+//               i.e. MN-major (loaded as two 64 x 64 boxes per 64-deep K slice).
+enum ProjMode : int { kPlain = 0, kGroupedK = 1, kGroupedMN = 2 };
+
+template <int BN, int kMode, class Ep>
 __global__ void __launch_bounds__(kThreads, 1)
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0,
                      const __grid_constant__ CUtensorMap tm_w1,
                      const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_x2, int m_tiles0, int O, int N,
-                     int k_chunks, int dual, Ep ep) {
+                     int k_chunks, int dual, int mt_group, int mt_cta, Ep ep) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -45,10 +53,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tile = blockIdx.x, n0 = blockIdx.y * BN;
-  const bool from_w1 = m_tile >= m_tiles0;
-  const int a_row = from_w1 ? (m_tile - m_tiles0) * 128 : m_tile * 128;
-  const int total_chunks = dual ? 2 * k_chunks : k_chunks;
+  const int n0 = blockIdx.y * BN;
+  const int m_first = blockIdx.x * mt_cta;
+  const int per_tile = dual ? 2 * k_chunks : k_chunks;
+  const int total_chunks = mt_cta * per_tile;
+  uint32_t tmem_cols = 32;  // a power of two >= the accumulator columns
+  while (tmem_cols < (uint32_t)(mt_cta * BN)) tmem_cols <<= 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -60,7 +70,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, BN < 32 ? 32 : BN);
+    tmem_alloc(tmem_slot, tmem_cols);
     tmem_relinquish();
   }
   __syncthreads();
@@ -72,52 +82,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch(&tm_w0);
     tma_prefetch(&tm_x);
     int issued = 0;
-    for (int kc = 0; kc < total_chunks; ++kc) {
-      const int s = kc % kStages, r = kc / kStages;
+    for (int g = 0; g < total_chunks; ++g) {
+      const int i = g / per_tile, kc = g % per_tile;
+      const int m_tile = m_first + i;
+      const int s = g % kStages, r = g / kStages;
       if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort)) break;
       uint8_t* a = smem + s * S::kStage;
       uint8_t* b = a + kTileA;
       mbar_arrive_expect_tx(&full[s], S::kStage);
       const int kx = (kc % k_chunks) * 64;
-      tma_load_2d(a, from_w1 ? &tm_w1 : &tm_w0, &full[s], kx, a_row);
-      tma_load_2d(b, (dual && kc >= k_chunks) ? &tm_x2 : &tm_x, &full[s], kx, n0);
+      const CUtensorMap* xm = (dual && kc >= k_chunks) ? &tm_x2 : &tm_x;
+      if (kMode == kPlain) {
+        const bool from_w1 = m_tile >= m_tiles0;
+        tma_load_2d(a, from_w1 ? &tm_w1 : &tm_w0, &full[s], kx,
+                    (from_w1 ? m_tile - m_tiles0 : m_tile) * 128);
+        tma_load_2d(b, xm, &full[s], kx, n0);
+      } else {
+        const int grp = m_tile / mt_group;
+        if (kMode == kGroupedK) {
+          tma_load_2d(a, &tm_w0, &full[s], kx, m_tile * 128);
+        } else {
+          const int col = (m_tile % mt_group) * 128, row = grp * k_chunks * 64 + kx;
+          tma_load_2d(a, &tm_w0, &full[s], col, row);
+          tma_load_2d(a + kTileA / 2, &tm_w0, &full[s], col + 64, row);
+        }
+        tma_load_3d(b, xm, &full[s], kx, grp, n0);
+      }
       ++issued;
     }
     // drain: every issued copy must land before the CTA may exit
-    for (int kc = (issued > kStages ? issued - kStages : 0); kc < issued; ++kc)
-      mbar_wait(&full[kc % kStages], (kc / kStages) & 1, abort);
+    for (int g = (issued > kStages ? issued - kStages : 0); g < issued; ++g)
+      mbar_wait(&full[g % kStages], (g / kStages) & 1, abort);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
-    constexpr uint32_t idesc = idesc_f16(128, BN, 1, 0, 0);
-    for (int kc = 0; kc < total_chunks; ++kc) {
-      const int s = kc % kStages, r = kc / kStages;
+    constexpr uint32_t idesc = idesc_f16(128, BN, 1, kMode == kGroupedMN ? 1 : 0, 0);
+    for (int g = 0; g < total_chunks; ++g) {
+      const int i = g / per_tile, kc = g % per_tile;
+      const int s = g % kStages, r = g / kStages;
       if (!mbar_wait(&full[s], r & 1, abort)) break;
       tc_fence_after();
       const uint32_t a = smem_u32(smem + s * S::kStage);
       const uint32_t b = a + kTileA;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_ss(tmem, smem_desc(a + kk * 32, 16, 1024), smem_desc(b + kk * 32, 16, 1024), idesc,
-               (kc | kk) != 0);
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t adesc = kMode == kGroupedMN ? smem_desc(a + kk * 2048, 8192, 1024)
+                                                   : smem_desc(a + kk * 32, 16, 1024);
+        mma_ss(tmem + i * BN, adesc, smem_desc(b + kk * 32, 16, 1024), idesc, (kc | kk) != 0);
+      }
       mma_commit(&empty[s]);
     }
     mma_commit(done);
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> registers -> global
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int o = (from_w1 ? m_tiles0 * 128 + a_row : a_row) + q * 32 + lane;
     if (mbar_wait(done, 0, abort)) {
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c, v);
-        tmem_wait_ld();
+      for (int i = 0; i < mt_cta; ++i) {
+        const int o = (m_first + i) * 128 + q * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + i * BN + c, v);
+          tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float vp = __shfl_xor_sync(0xffffffffu, v[j], 1);
-          const int n = n0 + c + j;
-          if (n < N && o < O) ep(o, n, v[j], vp);
+          for (int j = 0; j < 32; ++j) {
+            const float vp = __shfl_xor_sync(0xffffffffu, v[j], 1);
+            const int n = n0 + c + j;
+            if (n < N && o < O) ep(o, n, v[j], vp);
+          }
         }
       }
     }
@@ -126,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN < 32 ? 32 : BN);
+    tmem_dealloc(tmem, tmem_cols);
   }
 }
 
@@ -170,6 +203,12 @@ struct EpStoreBF16 {
     hi[(int64_t)n * ld + o] = h;
     if (lo) lo[(int64_t)n * ld + o] = __float2bfloat16_rn(v - __bfloat162float(h));
   }
+};
+
+struct EpStoreF32 {
+  float* y;
+  int64_t ld;
+  __device__ void operator()(int o, int n, float v, float) const { y[(int64_t)n * ld + o] = v; }
 };
 
 struct EpStoreF16 {
@@ -221,12 +260,12 @@ mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
   if (!tmap_rows(&tx2, a.X2 ? a.X2 : a.X, a.N, a.K, a.ldx, BN)) return MLA_ERR_CUDA;
   const int m_tiles = m0 + (a.W1 ? ceil_div(a.O1, 128) : 0);
   const uint32_t smem = ProjSmem<BN>::kBytes + 1024;
-  auto kern = proj_gemm_kernel<BN, Ep>;
+  auto kern = proj_gemm_kernel<BN, kPlain, Ep>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(m_tiles, ceil_div(a.N, BN));
   TraceScope ts(a.kid, st);
   kern<<<grid, kThreads, smem, st>>>(tw0, tw1, tx, tx2, m0, a.O0 + (a.W1 ? a.O1 : 0), a.N,
-                                     a.K / 64, a.X2 ? 1 : 0, ep);
+                                     a.K / 64, a.X2 ? 1 : 0, 1, 1, ep);
   return launch_status();
 }
 
@@ -238,6 +277,57 @@ mla_status_t launch_proj(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
   if (a.N <= 64) return launch_proj_bn<64>(a, ep, st);
   if (a.N <= 128) return launch_proj_bn<128>(a, ep, st);
   return launch_proj_bn<256>(a, ep, st);
+}
+
+// Grouped GEMM over heads: Y[n, g*Mg + m] = sum_k A_g[m, k] X[n, g, k] for g < G heads, with
+// A_g the head-g block of W ([G*Mg, K] row-major, kGroupedK) or of W^T (W [G*K, Mg]
+// row-major, kGroupedMN). X (and X2, accumulated against the same A) is [N, G, K] bf16.
+struct GroupArgs {
+  const void* W;
+  int G, Mg, K;
+  const void* X;
+  const void* X2;
+  int N;
+  int kid;
+};
+
+template <int BN, int kMode, class Ep>
+mla_status_t launch_grouped_bn(const GroupArgs& a, const Ep& ep, cudaStream_t st) {
+  CUtensorMap tw, tx, tx2;
+  if (kMode == kGroupedK) {
+    if (!tmap_rows(&tw, a.W, (int64_t)a.G * a.Mg, a.K, a.K, 128)) return MLA_ERR_CUDA;
+  } else {
+    if (!tmap_rows(&tw, a.W, (int64_t)a.G * a.K, a.Mg, a.Mg, 64)) return MLA_ERR_CUDA;
+  }
+  auto map3 = [&](CUtensorMap* m, const void* base) {
+    const uint64_t dims[3] = {(uint64_t)a.K, (uint64_t)a.G, (uint64_t)a.N};
+    const uint64_t strides[2] = {(uint64_t)a.K * 2, (uint64_t)a.G * a.K * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)BN};
+    return make_tmap(m, base, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  };
+  if (!map3(&tx, a.X) || !map3(&tx2, a.X2 ? a.X2 : a.X)) return MLA_ERR_CUDA;
+  const int mt_group = a.Mg / 128;
+  int mt_cta = mt_group;
+  while (mt_cta * BN > 512 || mt_group % mt_cta) --mt_cta;
+  const int m_tiles = a.G * mt_group;
+  const uint32_t smem = ProjSmem<BN>::kBytes + 1024;
+  auto kern = proj_gemm_kernel<BN, kMode, Ep>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  dim3 grid(m_tiles / mt_cta, ceil_div(a.N, BN));
+  TraceScope ts(a.kid, st);
+  kern<<<grid, kThreads, smem, st>>>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, a.K / 64,
+                                     a.X2 ? 1 : 0, mt_group, mt_cta, ep);
+  return launch_status();
+}
+
+template <int kMode, class Ep>
+mla_status_t launch_grouped(const GroupArgs& a, const Ep& ep, cudaStream_t st) {
+  if (a.N <= 0) return MLA_OK;
+  if (a.K % 64 || a.Mg % 128) return MLA_ERR_UNSUPPORTED;
+  if (a.N <= 32) return launch_grouped_bn<32, kMode>(a, ep, st);
+  if (a.N <= 64) return launch_grouped_bn<64, kMode>(a, ep, st);
+  if (a.N <= 128) return launch_grouped_bn<128, kMode>(a, ep, st);
+  return launch_grouped_bn<256, kMode>(a, ep, st);
 }
 
 }  // namespace
@@ -313,6 +403,23 @@ mla_status_t tc_expand(const void* W, int O, const void* latent, int64_t ld_late
   a.kid = kid;
   EpStoreF16 ep{(__half*)y, O};
   return launch_proj(a, ep, st);
+}
+
+// q~[b, i, :] = (W^UK_i)^T q^C[b, i, :]  ("从LLaMA到DeepSeek" §六): per head an MN-major
+// [d_c x d_h^C] block of W^UK against the B query rows of that head; bf16 out.
+mla_status_t tc_absorb(const mla_dims_t* d, const mla_weights_t* w, const void* q_c, int B,
+                       void* qt, int kid, cudaStream_t st) {
+  GroupArgs a{w->W_UK, d->n_h, d->d_c, d->d_hc, q_c, nullptr, B, kid};
+  EpStoreBF16 ep{(__nv_bfloat16*)qt, nullptr, (int64_t)d->n_h * d->d_c};
+  return launch_grouped<kGroupedMN>(a, ep, st);
+}
+
+// o[b, i, :] = W^UV_i o~[b, i, :] with o~ = hi + lo (two bf16 operands, one fp32 accumulator).
+mla_status_t tc_unabsorb(const mla_dims_t* d, const mla_weights_t* w, const void* ol_hi,
+                         const void* ol_lo, int B, float* o, int kid, cudaStream_t st) {
+  GroupArgs a{w->W_UV, d->n_h, d->d_hc, d->d_c, ol_hi, ol_lo, B, kid};
+  EpStoreF32 ep{o, (int64_t)d->n_h * d->d_hc};
+  return launch_grouped<kGroupedK>(a, ep, st);
 }
 
 }  // namespace mla

@@ -11,7 +11,7 @@ namespace mla {
 enum KernelId : int {
   K_APPEND = 0, K_Q_DOWN, K_Q_UP, K_ABSORB, K_DECODE_ATTN, K_DECODE_COMBINE, K_TOKEN_MAP,
   K_PREFILL_APPEND, K_PREFILL_Q_DOWN, K_PREFILL_Q_UP, K_EXPAND_K, K_EXPAND_V, K_PREFILL_ATTN,
-  K_NUM_IDS
+  K_DECODE_MERGE, K_UNABSORB, K_NUM_IDS
 };
 
 // Launch tracing (host side): while armed, trace_before/trace_after record caller-owned
@@ -56,6 +56,16 @@ mla_status_t tc_q_up(const mla_dims_t* d, const mla_weights_t* w, const void* cq
                      const void* cq_lo, const int32_t* pos, int n, void* q_c, void* q_r,
                      int64_t qc_tok, int64_t qc_head, int64_t qr_tok, int64_t qr_head,
                      bool f16_out, int kid, cudaStream_t st);
+mla_status_t tc_absorb(const mla_dims_t* d, const mla_weights_t* w, const void* q_c, int B,
+                       void* qt, int kid, cudaStream_t st);
+mla_status_t tc_unabsorb(const mla_dims_t* d, const mla_weights_t* w, const void* ol_hi,
+                         const void* ol_lo, int B, float* o, int kid, cudaStream_t st);
+
+// Tensor-core absorbed decode (V2 widths, bf16): decode_tc.cu
+size_t tc_decode_ws(const mla_dims_t* d, int B);
+mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* q_c,
+                       const void* q_r, const mla_cache_t* cache, const int32_t* seq_len, int B,
+                       int max_len, void* ws, float* o, cudaStream_t st);
 mla_status_t tc_expand(const void* W, int O, const void* latent, int64_t ld_latent, int K, int n,
                        void* y, int kid, cudaStream_t st);
 
