@@ -17,6 +17,7 @@ mla_status_t check_dims(const mla_dims_t* d) {
   if (!(d->rope_base > 0.f)) return MLA_ERR_INVALID_ARG;
   // RoPE rotates pairs; the pair-wise epilogues need even content widths too.
   if ((d->d_hr & 1) || (d->d_c & 1) || (d->d_hc & 1)) return MLA_ERR_UNSUPPORTED;
+  if (d->d_hr > 2 * kMaxRopePairs) return MLA_ERR_UNSUPPORTED;
   // vectorised row access: 16-byte row pitches of the cache and of every weight row
   const int v = d->dtype == MLA_BF16 ? 8 : 4;
   if ((d->d_c + d->d_hr) % v || d->d % v || d->d_cq % v || d->d_c % v) return MLA_ERR_UNSUPPORTED;

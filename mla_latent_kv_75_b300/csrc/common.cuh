@@ -37,15 +37,47 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 template <> __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
 
 // ----------------------------------------------------------------------------------
-// RoPE angle: pos * base^(-2k/d_r), reduced modulo 2*pi in double precision so that long
-// contexts (positions up to 2^31) keep full float accuracy in the rotation.
+// RoPE rotation for pair k at position pos: angle = pos * base^(-2k/d_r).
+// The frequencies are computed once on the host in double precision and handed to the
+// kernels as float pairs (f = hi + lo). The angle is formed in float-float arithmetic and
+// reduced modulo 2 pi by the Cody-Waite method (two-term 2 pi, fused multiply-adds), so that
+// long contexts keep float accuracy in the rotation without any double arithmetic on the
+// device. Positions are split into a multiple of 4096 and a remainder, both exact in float.
 // ----------------------------------------------------------------------------------
-__device__ __forceinline__ void rope_cs(int pos, int k, int d_r, float base, float* c, float* s) {
-  const double theta = pow((double)base, -2.0 * (double)k / (double)d_r);
-  const double two_pi = 6.283185307179586476925286766559;
-  double a = (double)pos * theta;
-  a = a - two_pi * floor(a / two_pi);
-  sincosf((float)a, s, c);
+constexpr int kMaxRopePairs = 64;  // d_h^R <= 128
+
+struct RopeFreqs {
+  float hi[kMaxRopePairs];
+  float lo[kMaxRopePairs];
+};
+
+inline RopeFreqs rope_freqs(const mla_dims_t* d) {
+  RopeFreqs f{};
+  for (int k = 0; k < d->d_hr / 2 && k < kMaxRopePairs; ++k) {
+    const double v = pow((double)d->rope_base, -2.0 * (double)k / (double)d->d_hr);
+    f.hi[k] = (float)v;
+    f.lo[k] = (float)(v - (double)f.hi[k]);
+  }
+  return f;
+}
+
+// pos * (fh + fl) reduced into [-pi, pi] (a few float ulps of pi)
+__device__ __forceinline__ float rope_reduce(float pos_part, float fh, float fl) {
+  constexpr float kInv2Pi = 0.15915494309189535f;
+  constexpr float k2PiHi = 6.28318548202514648f;     // float nearest to 2 pi
+  constexpr float k2PiLo = -1.7484556000744883e-7f;  // 2 pi - k2PiHi
+  const float a_hi = pos_part * fh;
+  const float a_lo = fmaf(pos_part, fh, -a_hi) + pos_part * fl;
+  const float n = rintf(a_hi * kInv2Pi);
+  float r = fmaf(-n, k2PiHi, a_hi);
+  r = fmaf(-n, k2PiLo, r);
+  return r + a_lo;
+}
+
+__device__ __forceinline__ void rope_cs(int pos, int k, const RopeFreqs& f, float* c, float* s) {
+  const float fh = f.hi[k], fl = f.lo[k];
+  const float r = rope_reduce((float)(pos & ~4095), fh, fl) + rope_reduce((float)(pos & 4095), fh, fl);
+  sincosf(r, s, c);
 }
 
 // ----------------------------------------------------------------------------------

@@ -9,17 +9,19 @@
 //   merge       log-sum-exp merge of the partials        o~[b,i,:] as a hi/lo bf16 pair
 //   unabsorb    o[b,i,:] = W^UV_i o~[b,i,:]              grouped tcgen05 GEMM (gemm_tc.cu)
 //
-// The attention kernel runs one cluster of two CTAs per pair of SMs. All 128 heads form the M
-// dimension of every MMA. The pair splits the 576-wide cache row: CTA 0 owns latent columns
-// [0, 256) plus the 64 RoPE columns, CTA 1 owns latent columns [256, 512). Each CTA
-//   - streams only its columns of each 64-row cache tile into shared memory with TMA,
-//   - computes its partial score S_r = Q_r K_r^T (K = 320 or 256; Q_r lives in TMEM),
-//   - sends S_r to the peer through distributed shared memory (st.async) and adds the peer's
-//     partial, so both CTAs hold the same full score tile,
-//   - runs the same online softmax (exp2, lazy rescaling) on it, writes P (bf16) to shared
-//     memory, and accumulates O_r += P V_r into TMEM, where V_r is the same shared-memory
-//     tile read as an MN-major operand (O_r is 128 heads x 256 latent columns, fp32).
-// No cache byte is read twice and no MMA work is duplicated across the pair.
+// Attention kernel. All 128 heads form the M dimension of every MMA. The accumulator
+// O~ (128 heads x 512 latent columns, fp32) would fill a whole SM's tensor memory, so two CTAs
+// (a "pair", on two SMs) share each piece of work: CTA r owns latent columns
+// [256 r, 256 r + 256) of O~. Both CTAs stream the full 576-wide cache tile and compute the
+// same score tile S = [q~ ; q^R] [c ; k^R]^T (K = 576) themselves: handing a score tile to
+// the other SM through distributed shared memory costs more time than recomputing it. The
+// query operand is split between tensor memory (K columns 0..383) and shared memory (K columns
+// 384..575), because the accumulator, the score tile and the whole query do not fit in the
+// 512 tensor-memory columns together. Per 48-row cache tile, per CTA:
+//   TMA     9 boxes of 64 columns x 48 rows into a 3-deep shared-memory ring
+//   MMA     S = Q K^T (36 K-steps of 16) into tensor memory; later O_r += P V_r (3 K-steps)
+//   softmax one thread per head: online softmax in log2 units with lazy rescaling, P in bf16
+// Both CTAs of a pair therefore hold bitwise identical scores and softmax statistics.
 //
 // Work split: the cache tiles of all sequences form one list (sequence by sequence); pair p of
 // P takes the contiguous range [p*T/P, (p+1)*T/P). Every (sequence b, pair p) intersection is
@@ -40,33 +42,36 @@ namespace {
 constexpr int kDC = 512;          // d_c
 constexpr int kRowElems = 576;    // d_c + d_h^R
 constexpr int kHeads = 128;       // n_h
-constexpr int kTile = 64;         // cache rows per tile
-constexpr int kStages = 4;
-constexpr int kBox = 64 * 64 * 2;  // one TMA box: 64 columns x 64 rows of bf16 (8 KB)
-constexpr int kStageBytes = 5 * kBox;
-constexpr int kPBytes = kHeads * kTile * 2;  // P tile, bf16
-constexpr int kXBytes = kHeads * kTile * 4;  // partial-score exchange tile, fp32
-constexpr int kOffP = kStages * kStageBytes;
-constexpr int kOffX = kOffP + 2 * kPBytes;
-constexpr int kOffBar = kOffX + kXBytes;
-constexpr int kThreads = 192;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
-constexpr int kMaxPairs = 80;  // partial slots are sized for at most this many SM pairs
+constexpr int kTile = 48;         // cache rows per tile
+constexpr int kStages = 3;
+constexpr int kBox = 64 * kTile * 2;   // one TMA box: 64 columns x 48 rows of bf16 (6 KB)
+constexpr int kStageBytes = 9 * kBox;  // the whole 576-wide tile
+constexpr int kQBox = 64 * kHeads * 2; // 64 query columns x 128 heads (16 KB)
+constexpr int kQTmemK = 384;           // query K columns held in tensor memory
+constexpr int kOffQb = 0;              // query K columns 384..575 (3 boxes)
+constexpr int kOffStage = 3 * kQBox;
+constexpr int kPBytes = kHeads * 128;  // P: one 128-byte swizzled row per head (48 used)
+constexpr int kOffP = kOffStage + kStages * kStageBytes;
+constexpr int kOffBar = kOffP + kPBytes;
+constexpr int kThreads = 224;  // 7 warps: 0 TMA (score-only boxes), 1 MMA, 2..5 softmax, 6 TMA (V boxes)
+constexpr int kSmemUsed = kOffBar + 256;
+constexpr int kSmemBytes = 232448;  // the opt-in maximum; the base is aligned up to 1 KB
+constexpr int kMaxPairs = 80;       // partial slots are sized for at most this many CTA pairs
+static_assert(kBox % 1024 == 0 && kOffStage % 1024 == 0 && kOffP % 1024 == 0, "1 KB alignment");
 
 // tensor-memory columns
 constexpr uint32_t kColO = 0;    // O_r: 256 fp32 columns
-constexpr uint32_t kColS = 256;  // S tile: 64 fp32 columns
-constexpr uint32_t kColQ = 320;  // Q_r: 160 (rank 0) or 128 (rank 1) columns of bf16 pairs
+constexpr uint32_t kColS = 256;  // S tile: 48 fp32 columns
+constexpr uint32_t kColQ = 320;  // Q K-columns 0..383: 192 columns of bf16 pairs
 
 constexpr float kTau = 8.f;  // lazy rescale threshold (log2 units): p <= 2^8 between rescales
 
 struct Shared {
-  uint64_t full[kStages], empty[kStages];
-  uint64_t s_full, s_free, p_full[2], pv_done, x_full, x_empty, q_full;
+  uint64_t full[kStages], empty_a[kStages], empty_b[kStages];
+  uint64_t s_full, s_free, p_full, pv_done, q_full;
   uint32_t tmem_slot;
   int abort;
   int b0, j0;
-  long long t_begin, t_end;
   long long red[8];
 };
 static_assert(sizeof(Shared) <= 256, "barrier block");
@@ -157,31 +162,6 @@ struct Cursor {
   }
 };
 
-// Warp-uniform bounded wait used by the softmax warps (every lane polls; the warp leaves
-// together, either when all lanes saw the phase complete or on timeout / abort).
-template <bool kCluster>
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  uint64_t t0 = 0;
-  for (int it = 0;; ++it) {
-    const bool ok = kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, ok)) return true;
-    if ((it & 63) == 63) {
-      int stop = 0;
-      if ((threadIdx.x & 31) == 0) {
-        if (t0 == 0) t0 = global_ns();
-        if (*abort) {
-          stop = 1;
-        } else if (global_ns() - t0 > kWaitLimitNs) {
-          flag_status(MLA_ERR_TIMEOUT);
-          *abort = 1;
-          stop = 1;
-        }
-      }
-      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
-    }
-  }
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -192,8 +172,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // ------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
     decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_rows,
-                          const __nv_bfloat16* __restrict__ qt,   // [B, 128, 512]
-                          const __nv_bfloat16* __restrict__ q_r,  // [B, 128, 64]
+                          const __grid_constant__ CUtensorMap tm_qt,  // q~ [B*128, 512]
+                          const __grid_constant__ CUtensorMap tm_qr,  // q^R [B*128, 64]
+                          const __nv_bfloat16* __restrict__ qt,       // [B, 128, 512]
                           const int32_t* __restrict__ seq_len,
                           const int64_t* __restrict__ seq_base, int64_t capacity, int B,
                           int max_len, float scale_log2, float* __restrict__ part_o,
@@ -204,22 +185,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   Shared& sh = *reinterpret_cast<Shared*>(smem + kOffBar);
   volatile int* abort = &sh.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
+  const int rank = blockIdx.x & 1;  // latent half owned by this CTA
   const int P = gridDim.x / 2, p = blockIdx.x / 2;
-  const int nbox = rank == 0 ? 5 : 4;
+  // the aligned layout must fit in the allocation (it does when the base is 1 KB aligned)
+  if ((smem - smem_raw) + kSmemUsed > kSmemBytes) {
+    if (threadIdx.x == 0) flag_status(MLA_ERR_UNSUPPORTED);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], 1);
+      mbar_init(&sh.full[s], 2);  // one arrival per producer, plus the bytes of all 9 boxes
+      mbar_init(&sh.empty_a[s], 1);
+      mbar_init(&sh.empty_b[s], 1);
     }
     mbar_init(&sh.s_full, 1);
     mbar_init(&sh.s_free, 4);
-    mbar_init(&sh.p_full[0], 4);
-    mbar_init(&sh.p_full[1], 4);
+    mbar_init(&sh.p_full, 4);
     mbar_init(&sh.pv_done, 1);
-    mbar_init(&sh.x_full, 1);
-    mbar_init(&sh.x_empty, 4);
     mbar_init(&sh.q_full, 4);
     sh.abort = 0;
     sh.b0 = 0;
@@ -230,7 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&sh.tmem_slot, 512);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) tma_prefetch(&tm_rows);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tm_rows);
+    tma_prefetch(&tm_qt);
+    tma_prefetch(&tm_qr);
+  }
 
   // ---- plan: total tile count T, this pair's range and its first (sequence, tile)
   long long local = 0;
@@ -255,117 +242,137 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  cluster_sync();  // the peer's barriers are initialised before any remote arrive / st.async
   tc_fence_after();
   const uint32_t tmem = sh.tmem_slot;
   const int nt = (int)(t_end - t_begin);
+  uint8_t* const qb = smem + kOffQb;
+  uint8_t* const pbuf = smem + kOffP;
 
-  if (nt > 0 && warp == 0 && lane == 0) {
-    // ------------------------------------------------------------- TMA producer
+  if (nt > 0 && (warp == 0 || warp == 6) && lane == 0) {
+    // ------------------------------------------------------------- TMA producers
+    // Warp 0 loads the boxes only the score MMA reads (the other CTA's latent half and the RoPE
+    // columns); they are released as soon as the score MMA of their tile completes. Warp 6 loads
+    // this CTA's V half, released after the PV MMA. Both walk the same tile sequence.
+    const bool v_boxes = warp == 6;
+    uint64_t* empty = v_boxes ? sh.empty_b : sh.empty_a;
     Cursor cur{sh.b0, sh.j0, seq_info(seq_len, seq_base, sh.b0, max_len, capacity, false)};
     int issued = 0;
     for (int t = 0; t < nt; ++t) {
       const int s = t % kStages, r = t / kStages;
-      if (r > 0 && !mbar_wait(&sh.empty[s], (r - 1) & 1, abort)) break;
-      uint8_t* stage = smem + s * kStageBytes;
-      mbar_arrive_expect_tx(&sh.full[s], nbox * kBox);
+      if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort)) break;
+      uint8_t* stage = smem + kOffStage + s * kStageBytes;
+      mbar_arrive_expect_tx(&sh.full[s], (v_boxes ? 4 : 5) * kBox);
       const int y = (int)(cur.s.base + (int64_t)cur.j * kTile);
-      for (int k = 0; k < nbox; ++k) {
-        const int x = rank == 0 ? (k < 4 ? k * 64 : kDC) : 256 + k * 64;
-        tma_load_2d(stage + k * kBox, &tm_rows, &sh.full[s], x, y);
+#pragma unroll 1
+      for (int k = 0; k < 9; ++k) {
+        const bool is_v = (k >> 2) == rank && k < 8;
+        if (is_v == v_boxes) tma_load_2d(stage + k * kBox, &tm_rows, &sh.full[s], k * 64, y);
       }
       ++issued;
       if (t + 1 < nt) cur.next(seq_len, seq_base, max_len, capacity);
     }
     for (int t = (issued > kStages ? issued - kStages : 0); t < issued; ++t)
       mbar_wait(&sh.full[t % kStages], (t / kStages) & 1, abort);
-  } else if (nt > 0 && warp == 1 && lane == 0) {
-    // ------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc_s = idesc_f16(128, 64, 1, 0, 0);
+  } else if (nt > 0 && warp == 1) {
+    // ------------------------------------------------------------- MMA issuer (one elected
+    // lane of a converged warp; the descriptors are precomputed and the K loops unrolled)
+    constexpr uint32_t idesc_s = idesc_f16(128, kTile, 1, 0, 0);
     constexpr uint32_t idesc_o = idesc_f16(128, 256, 1, 0, 1);
-    const int nks = rank == 0 ? 20 : 16;  // 16-wide K steps of the score MMA
     Cursor cur{sh.b0, sh.j0, seq_info(seq_len, seq_base, sh.b0, max_len, capacity, false)};
     int seg = 0;
-    bool ok = true;
+    const uint64_t desc_qb = smem_desc(smem_u32(qb), 16, 1024);
+    const uint64_t desc_p = smem_desc(smem_u32(pbuf), 16, 1024);
+    const uint64_t desc_st = smem_desc(smem_u32(smem + kOffStage), 16, 1024);
+    const uint64_t desc_v = smem_desc(smem_u32(smem + kOffStage + 4 * rank * kBox), kBox, 1024);
     auto issue_s = [&](int t) -> bool {
       const int s = t % kStages;
-      if (!mbar_wait(&sh.full[s], (t / kStages) & 1, abort)) return false;
+      if (!warp_wait(&sh.full[s], (t / kStages) & 1, abort)) return false;
       tc_fence_after();
-      const uint32_t st = smem_u32(smem + s * kStageBytes);
-      for (int ks = 0; ks < nks; ++ks)
-        mma_ts(tmem + kColS, tmem + kColQ + ks * 8,
-               smem_desc(st + (ks >> 2) * kBox + (ks & 3) * 32, 16, 1024), idesc_s, ks > 0);
-      mma_commit(&sh.s_full);
+      if (elect_one()) {
+        const uint64_t bst = desc_st + (uint64_t)((s * kStageBytes) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < 36; ++ks) {
+          const uint64_t bdesc = bst + (uint64_t)(((ks >> 2) * kBox + (ks & 3) * 32) >> 4);
+          if (ks < kQTmemK / 16)
+            mma_ts(tmem + kColS, tmem + kColQ + ks * 8, bdesc, idesc_s, ks > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem + kColS,
+                   desc_qb + (uint64_t)((((ks - 24) >> 2) * kQBox + (ks & 3) * 32) >> 4), bdesc,
+                   idesc_s, 1u);
+        }
+        mma_commit(&sh.s_full);
+        mma_commit(&sh.empty_a[s]);
+      }
+      __syncwarp();
       return true;
     };
-    ok = mbar_wait(&sh.q_full, 0, abort) && (tc_fence_after(), issue_s(0));
+    bool ok = warp_wait(&sh.q_full, 0, abort);
+    if (ok) {
+      tc_fence_after();
+      ok = issue_s(0);
+    }
     for (int t = 0; ok && t < nt; ++t) {
       const bool last_in_seg = cur.j + 1 == cur.s.n;
       const bool seg_first = t == 0 || cur.j == 0;  // O starts from zero
       if (t + 1 < nt && !last_in_seg) {
-        if (!mbar_wait(&sh.s_free, t & 1, abort) || !issue_s(t + 1)) break;
+        if (!warp_wait(&sh.s_free, t & 1, abort) || !issue_s(t + 1)) break;
       }
-      if (!mbar_wait(&sh.p_full[t & 1], (t >> 1) & 1, abort)) break;
+      if (!warp_wait(&sh.p_full, t & 1, abort)) break;
       tc_fence_after();
-      const uint32_t st = smem_u32(smem + (t % kStages) * kStageBytes);
-      const uint32_t pb = smem_u32(smem + kOffP + (t & 1) * kPBytes);
+      if (elect_one()) {
+        const uint64_t bv = desc_v + (uint64_t)(((t % kStages) * kStageBytes) >> 4);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tmem + kColO, smem_desc(pb + ks * 32, 16, 1024),
-               smem_desc(st + ks * 2048, 8192, 1024), idesc_o, (!seg_first || ks > 0) ? 1u : 0u);
-      mma_commit(&sh.empty[t % kStages]);
-      mma_commit(&sh.pv_done);
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          mma_ss(tmem + kColO, desc_p + (uint64_t)((ks * 32) >> 4),
+                 bv + (uint64_t)((ks * 2048) >> 4), idesc_o, (!seg_first || ks > 0) ? 1u : 0u);
+        mma_commit(&sh.empty_b[t % kStages]);
+        mma_commit(&sh.pv_done);
+      }
+      __syncwarp();
       if (t + 1 < nt && last_in_seg) {
         ++seg;
-        if (!mbar_wait(&sh.q_full, seg & 1, abort) || !mbar_wait(&sh.s_free, t & 1, abort))
+        if (!warp_wait(&sh.q_full, seg & 1, abort) || !warp_wait(&sh.s_free, t & 1, abort))
           break;
         tc_fence_after();
         if (!issue_s(t + 1)) break;
       }
       if (t + 1 < nt) cur.next(seq_len, seq_base, max_len, capacity);
     }
-  } else if (nt > 0 && warp >= 2) {
+  } else if (nt > 0 && warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------- softmax warps
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int h = q * 32 + lane;            // head = TMEM lane
     const int ts = threadIdx.x - 64;        // 0..127 among the softmax threads
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    uint8_t* X = smem + kOffX;
-    const uint32_t peer = rank ^ 1u;
-    const uint32_t peer_x = mapa_shared(smem_u32(X), peer) + h * 256;
-    const uint32_t peer_xfull = mapa_shared(smem_u32(&sh.x_full), peer);
-    const uint32_t peer_xempty = mapa_shared(smem_u32(&sh.x_empty), peer);
     const int sw = h & 7;
 
-    // Q_r of sequence b into TMEM (two bf16 per column)
+    // Query of sequence b: K columns 0..383 into tensor memory (two bf16 per column, one
+    // thread per head), K columns 384..575 into shared memory by TMA.
     auto load_q = [&](int b) {
-      const uint4* src = reinterpret_cast<const uint4*>(qt + ((int64_t)b * kHeads + h) * kDC +
-                                                        rank * 256);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {  // 4 x 32 columns = 256 bf16
-        uint32_t r[32];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 v = src[c * 8 + k];
-          r[4 * k] = v.x;
-          r[4 * k + 1] = v.y;
-          r[4 * k + 2] = v.z;
-          r[4 * k + 3] = v.w;
-        }
-        tmem_st32u(lane_base + kColQ + c * 32, r);
+      if (ts == 0) {
+        mbar_expect_tx(&sh.q_full, 3 * kQBox);
+        tma_load_2d(qb, &tm_qt, &sh.q_full, 384, b * kHeads);
+        tma_load_2d(qb + kQBox, &tm_qt, &sh.q_full, 448, b * kHeads);
+        tma_load_2d(qb + 2 * kQBox, &tm_qr, &sh.q_full, 0, b * kHeads);
       }
-      if (rank == 0) {  // q^R: 64 bf16 = 32 columns
-        const uint4* sr = reinterpret_cast<const uint4*>(q_r + ((int64_t)b * kHeads + h) * 64);
-        uint32_t r[32];
+      const uint4* src = reinterpret_cast<const uint4*>(qt + ((int64_t)b * kHeads + h) * kDC);
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint4 v[24];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 v = sr[k];
-          r[4 * k] = v.x;
-          r[4 * k + 1] = v.y;
-          r[4 * k + 2] = v.z;
-          r[4 * k + 3] = v.w;
+        for (int k = 0; k < 24; ++k) v[k] = __ldg(src + half * 24 + k);
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            r[4 * k] = v[c * 8 + k].x;
+            r[4 * k + 1] = v[c * 8 + k].y;
+            r[4 * k + 2] = v[c * 8 + k].z;
+            r[4 * k + 3] = v[c * 8 + k].w;
+          }
+          tmem_st32u(lane_base + kColQ + (half * 3 + c) * 32, r);
         }
-        tmem_st32u(lane_base + kColQ + 128, r);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -379,48 +386,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < nt; ++t) {
       const int j = cur.j;
       const int valid = min(kTile, cur.s.L - j * kTile);
-      float s[64];
-      if (!warp_wait<false>(&sh.s_full, t & 1, abort)) break;
+      float s[kTile];
+      if (!warp_wait(&sh.s_full, t & 1, abort)) break;
       tc_fence_after();
       tmem_ld32(lane_base + kColS, *reinterpret_cast<float(*)[32]>(&s[0]));
-      tmem_ld32(lane_base + kColS + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+      tmem_ld16(lane_base + kColS + 32, &s[32]);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.s_free);
 
-      // exchange partial scores with the peer CTA
-      if (t > 0 && !warp_wait<true>(&sh.x_empty, (t - 1) & 1, abort)) break;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_async_v4(peer_x + ((c ^ sw) << 4), peer_xfull, s[4 * c], s[4 * c + 1], s[4 * c + 2],
-                    s[4 * c + 3]);
-      if (ts == 0) mbar_arrive_expect_tx(&sh.x_full, kXBytes);
-      if (!warp_wait<true>(&sh.x_full, t & 1, abort)) break;
-      const uint8_t* xrow = X + h * 256;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 v = *reinterpret_cast<const float4*>(xrow + ((c ^ sw) << 4));
-        s[4 * c] += v.x;
-        s[4 * c + 1] += v.y;
-        s[4 * c + 2] += v.z;
-        s[4 * c + 3] += v.w;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(peer_xempty);
-
       // online softmax in log2 units with lazy rescaling
-      float mt = -INFINITY;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        s[i] = i < valid ? s[i] * scale_log2 : -INFINITY;
-        mt = fmaxf(mt, s[i]);
-      }
+      for (int i = 0; i < kTile; ++i)
+        if (i < valid) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
       const bool first = t == 0 || j == 0;  // first tile of a segment
       const float m_new = first ? mt : (mt > m_used + kTau ? mt : m_used);
-      const float alpha = first ? 0.f : exp2f(m_used - m_new);
-      if (__any_sync(0xffffffffu, !first && m_new != m_used)) {
-        if (!warp_wait<false>(&sh.pv_done, (t - 1) & 1, abort)) break;
+      const float alpha = first ? 0.f : ex2(m_used - m_new);
+      m_used = m_new;
+
+      // P in bf16 (and its row sum) while the previous tile's PV may still run
+      uint32_t w[kTile / 2];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < kTile / 2; ++k) {
+        const int i = 2 * k;
+        const float p0 = i < valid ? ex2(fmaf(s[i], scale_log2, -m_used)) : 0.f;
+        const float p1 = i + 1 < valid ? ex2(fmaf(s[i + 1], scale_log2, -m_used)) : 0.f;
+        w[k] = pack_bf16(p0, p1);
+        const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+        ls[k & 3] += __low2float(pb) + __high2float(pb);
+      }
+      l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+
+      // P and O are free once the previous tile's PV has completed
+      if (t > 0 && !warp_wait(&sh.pv_done, (t - 1) & 1, abort)) break;
+      if (__any_sync(0xffffffffu, alpha != 1.f && !first)) {
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
@@ -433,58 +436,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
       }
-      l_sum *= alpha;
-      m_used = m_new;
-
-      // P (bf16) -> shared memory, K-major with the 128-byte swizzle
-      uint8_t* prow = smem + kOffP + (t & 1) * kPBytes + h * 128;
+      // P -> shared memory, K-major with the 128-byte swizzle
+      uint8_t* prow = pbuf + h * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float p0 = exp2f(s[8 * c + 2 * k] - m_used);
-          const float p1 = exp2f(s[8 * c + 2 * k + 1] - m_used);
-          w[k] = pack_bf16(p0, p1);
-          const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
-          l_sum += __low2float(pb) + __high2float(pb);
-        }
-        *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
+      for (int c = 0; c < kTile / 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
       if (valid < kTile) {
         // rows past the sequence end may hold anything (even NaN): zero them in the V operand
-        uint8_t* stage = smem + (t % kStages) * kStageBytes;
+        uint8_t* v0 = smem + kOffStage + (t % kStages) * kStageBytes + 4 * rank * kBox;
         const int n16 = (kTile - valid) * 8;  // 16-byte chunks per box
         for (int e = ts; e < 4 * n16; e += 128) {
           const int box = e / n16, r = e % n16;
-          *reinterpret_cast<uint4*>(stage + box * kBox + valid * 128 + r * 16) =
+          *reinterpret_cast<uint4*>(v0 + box * kBox + valid * 128 + r * 16) =
               make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.p_full[t & 1]);
+      if (lane == 0) mbar_arrive(&sh.p_full);
 
       if (j + 1 == cur.s.n || t + 1 == nt) {
         // end of a segment (end of the sequence or of this pair's range): the next
-        // sequence's Q first, then O_r and (m, l) to the segment's partial slot
+        // sequence's query first, then O_r and (m, l) to the segment's partial slot
         const int b_done = cur.b;
         if (t + 1 < nt) {
           cur.next(seq_len, seq_base, max_len, capacity);
           load_q(cur.b);
         }
-        if (!warp_wait<false>(&sh.pv_done, t & 1, abort)) break;
+        if (!warp_wait(&sh.pv_done, t & 1, abort)) break;
         tc_fence_after();
         const int64_t slot = (int64_t)b_done + p;
-        float* dst = part_o + (slot * kDC + rank * 256) * kHeads + h;
+        float4* dst = reinterpret_cast<float4*>(part_o + (slot * kHeads + h) * kDC + rank * 256);
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
           float o[32];
           tmem_ld32(lane_base + kColO + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) dst[(int64_t)(c * 32 + k) * kHeads] = o[k];
+          for (int k = 0; k < 8; ++k)
+            dst[c * 8 + k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
         }
         if (rank == 0) {
           part_ml[slot * 256 + h] = m_used;
@@ -504,7 +496,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  cluster_sync();  // no CTA leaves while the peer may still address its shared memory
 }
 
 // ------------------------------------------------------------------------------------------
@@ -549,9 +540,15 @@ __global__ void __launch_bounds__(kMergeThreads)
       const int64_t slot = (int64_t)b + pp;
       const float w = exp2f(part_ml[slot * 256 + h] - M);
       lsum += w * part_ml[slot * 256 + 128 + h];
-      const float* src = part_o + (slot * kDC + c0) * kHeads + h;
+      const float4* src = reinterpret_cast<const float4*>(part_o + (slot * kHeads + h) * kDC + c0);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = fmaf(w, src[(int64_t)i * kHeads], acc[i]);
+      for (int i = 0; i < 8; ++i) {
+        const float4 v = src[i];
+        acc[4 * i] = fmaf(w, v.x, acc[4 * i]);
+        acc[4 * i + 1] = fmaf(w, v.y, acc[4 * i + 1]);
+        acc[4 * i + 2] = fmaf(w, v.z, acc[4 * i + 2]);
+        acc[4 * i + 3] = fmaf(w, v.w, acc[4 * i + 3]);
+      }
     }
     inv_l = lsum > 0.f ? 1.f / lsum : 0.f;
   }
@@ -596,23 +593,8 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int g_pairs[kMaxDevices] = {};
 
-cudaLaunchConfig_t attn_config(int pairs, cudaStream_t st, cudaLaunchAttribute* attr) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = st;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
-}
-
-// Number of CTA pairs that are resident at once on the current device (one pair per two SMs
-// that can host a 2-CTA cluster), capped at kMaxPairs. Set up once per device.
+// Number of CTA pairs resident at once on the current device (one CTA per SM), capped at
+// kMaxPairs. Set up once per device.
 mla_status_t attn_pairs(int* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
@@ -622,11 +604,14 @@ mla_status_t attn_pairs(int* out) {
     if (cudaFuncSetAttribute(decode_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
       return MLA_ERR_CUDA;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = attn_config(kMaxPairs, nullptr, attr);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_attn_tc_kernel, &cfg) != cudaSuccess || n < 1)
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_attn_tc_kernel, kThreads,
+                                                      kSmemBytes) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        per_sm < 1)
       return MLA_ERR_CUDA;
+    const int n = per_sm * sms / 2;
+    if (n < 1) return MLA_ERR_UNSUPPORTED;
     g_pairs[dev] = n < kMaxPairs ? n : kMaxPairs;
   }
   *out = g_pairs[dev];
@@ -657,20 +642,36 @@ mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* 
 
   // 2. attention over the latent cache
   if (max_len > 0 && cache->capacity > 0) {
-    CUtensorMap tm;
-    const uint64_t dims[2] = {(uint64_t)kRowElems, (uint64_t)cache->capacity};
-    const uint64_t strides[1] = {(uint64_t)kRowElems * 2};
-    const uint32_t box[2] = {64, (uint32_t)kTile};
-    if (!make_tmap(&tm, cache->rows, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
-      return MLA_ERR_CUDA;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = attn_config(pairs, st, attr);
+    CUtensorMap tm_rows, tm_qt, tm_qr;
+    {
+      const uint64_t dims[2] = {(uint64_t)kRowElems, (uint64_t)cache->capacity};
+      const uint64_t strides[1] = {(uint64_t)kRowElems * 2};
+      const uint32_t box[2] = {64, (uint32_t)kTile};
+      if (!make_tmap(&tm_rows, cache->rows, 2, dims, strides, box,
+                     CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+        return MLA_ERR_CUDA;
+    }
+    {
+      const uint64_t dims[2] = {(uint64_t)kDC, (uint64_t)B * kHeads};
+      const uint64_t strides[1] = {(uint64_t)kDC * 2};
+      const uint32_t box[2] = {64, (uint32_t)kHeads};
+      if (!make_tmap(&tm_qt, qt, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+        return MLA_ERR_CUDA;
+    }
+    {
+      const uint64_t dims[2] = {64, (uint64_t)B * kHeads};
+      const uint64_t strides[1] = {64 * 2};
+      const uint32_t box[2] = {64, (uint32_t)kHeads};
+      if (!make_tmap(&tm_qr, q_r, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+        return MLA_ERR_CUDA;
+    }
     const float scale_log2 = softmax_scale(d) * 1.4426950408889634f;
     TraceScope ts(K_DECODE_ATTN, st);
-    if (cudaLaunchKernelEx(&cfg, decode_attn_tc_kernel, tm, (const __nv_bfloat16*)qt,
-                           (const __nv_bfloat16*)q_r, seq_len, cache->seq_base, cache->capacity,
-                           B, max_len, scale_log2, part, ml) != cudaSuccess)
-      return MLA_ERR_CUDA;
+    decode_attn_tc_kernel<<<2 * pairs, kThreads, kSmemBytes, st>>>(
+        tm_rows, tm_qt, tm_qr, (const __nv_bfloat16*)qt, seq_len, cache->seq_base,
+        cache->capacity, B, max_len, scale_log2, part, ml);
+    s = launch_status();
+    if (s != MLA_OK) return s;
   }
 
   // 3. merge the partials of each sequence (o~ = 0 for empty sequences)

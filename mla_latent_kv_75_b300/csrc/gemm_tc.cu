@@ -113,25 +113,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     // drain: every issued copy must land before the CTA may exit
     for (int g = (issued > kStages ? issued - kStages : 0); g < issued; ++g)
       mbar_wait(&full[g % kStages], (g / kStages) & 1, abort);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (one elected lane of the converged warp)
     constexpr uint32_t idesc = idesc_f16(128, BN, 1, kMode == kGroupedMN ? 1 : 0, 0);
+    const uint64_t a0 = kMode == kGroupedMN ? smem_desc(smem_u32(smem), 8192, 1024)
+                                            : smem_desc(smem_u32(smem), 16, 1024);
+    const uint64_t b0 = smem_desc(smem_u32(smem) + kTileA, 16, 1024);
     for (int g = 0; g < total_chunks; ++g) {
       const int i = g / per_tile, kc = g % per_tile;
       const int s = g % kStages, r = g / kStages;
-      if (!mbar_wait(&full[s], r & 1, abort)) break;
+      if (!warp_wait(&full[s], r & 1, abort)) break;
       tc_fence_after();
-      const uint32_t a = smem_u32(smem + s * S::kStage);
-      const uint32_t b = a + kTileA;
+      if (elect_one()) {
+        const uint64_t off = (uint64_t)((s * S::kStage) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t adesc = kMode == kGroupedMN ? smem_desc(a + kk * 2048, 8192, 1024)
-                                                   : smem_desc(a + kk * 32, 16, 1024);
-        mma_ss(tmem + i * BN, adesc, smem_desc(b + kk * 32, 16, 1024), idesc, (kc | kk) != 0);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t adesc = a0 + off + (uint64_t)((kMode == kGroupedMN ? kk * 2048 : kk * 32) >> 4);
+          mma_ss(tmem + i * BN, adesc, b0 + off + (uint64_t)((kk * 32) >> 4), idesc,
+                 (kc | kk) != 0 ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
       }
-      mma_commit(&empty[s]);
+      __syncwarp();
     }
-    mma_commit(done);
+    if (elect_one()) mma_commit(done);
+    __syncwarp();
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> registers -> global
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -173,13 +179,13 @@ struct EpAppend {
   const int32_t* seq_idx;
   const int32_t* pos;
   __nv_bfloat16* packed;  // [N, pitch] or null
-  int d_c, d_hr;
-  float base;
+  int d_c;
+  RopeFreqs rf;
   __device__ void operator()(int o, int n, float v, float vp) const {
     const int p = pos[n];
     if (o >= d_c) {
       float c, s;
-      rope_cs(p, (o - d_c) >> 1, d_hr, base, &c, &s);
+      rope_cs(p, (o - d_c) >> 1, rf, &c, &s);
       v = ((o - d_c) & 1) ? (vp * s + v * c) : (v * c - vp * s);
     }
     const __nv_bfloat16 b = __float2bfloat16_rn(v);
@@ -227,7 +233,7 @@ struct EpQuery {
   int64_t qc_tok, qc_head, qr_tok, qr_head;
   const int32_t* pos;
   int n_h, d_hc, d_hr;
-  float base;
+  RopeFreqs rf;
   __device__ void operator()(int o, int n, float v, float vp) const {
     const int nc = n_h * d_hc;
     if (o < nc) {
@@ -235,7 +241,7 @@ struct EpQuery {
     } else {
       const int r = o - nc, i = r / d_hr, e = r % d_hr;
       float c, s;
-      rope_cs(pos[n], e >> 1, d_hr, base, &c, &s);
+      rope_cs(pos[n], e >> 1, rf, &c, &s);
       v = (e & 1) ? (vp * s + v * c) : (v * c - vp * s);
       q_r[n * qr_tok + i * qr_head + e] = from_f<T>(v);
     }
@@ -347,8 +353,7 @@ mla_status_t tc_append(const mla_dims_t* d, const mla_weights_t* w, const void* 
   a.N = n;
   a.kid = kid;
   EpAppend ep{(__nv_bfloat16*)cache->rows, (int64_t)(d->d_c + d->d_hr), cache->capacity,
-              cache->seq_base, seq_idx, pos, (__nv_bfloat16*)packed, d->d_c, d->d_hr,
-              d->rope_base};
+              cache->seq_base, seq_idx, pos, (__nv_bfloat16*)packed, d->d_c, rope_freqs(d)};
   return launch_proj(a, ep, st);
 }
 
@@ -383,11 +388,11 @@ mla_status_t tc_q_up(const mla_dims_t* d, const mla_weights_t* w, const void* cq
   a.kid = kid;
   if (f16_out) {
     EpQuery<__half> ep{(__half*)q_c, (__half*)q_r, qc_tok, qc_head, qr_tok, qr_head, pos,
-                       d->n_h, d->d_hc, d->d_hr, d->rope_base};
+                       d->n_h, d->d_hc, d->d_hr, rope_freqs(d)};
     return launch_proj(a, ep, st);
   }
   EpQuery<__nv_bfloat16> ep{(__nv_bfloat16*)q_c, (__nv_bfloat16*)q_r, qc_tok, qc_head, qr_tok,
-                            qr_head, pos, d->n_h, d->d_hc, d->d_hr, d->rope_base};
+                            qr_head, pos, d->n_h, d->d_hc, d->d_hr, rope_freqs(d)};
   return launch_proj(a, ep, st);
 }
 

@@ -89,8 +89,8 @@ struct AppendEp {
   const int64_t* seq_base;
   const int32_t* seq_idx;  // null: token n belongs to tok_seq[n]
   const int32_t* pos;
-  int d_c, d_hr;
-  float base;
+  int d_c;
+  RopeFreqs rf;
   __device__ void operator()(int n, int o, float a0, float a1) const {
     const int p = pos[n];
     const int64_t row = seq_base[seq_idx[n]] + p;
@@ -100,7 +100,7 @@ struct AppendEp {
     }
     if (o >= d_c) {  // k^R pair (2k, 2k+1) of the decoupled RoPE key
       float c, s;
-      rope_cs(p, (o - d_c) >> 1, d_hr, base, &c, &s);
+      rope_cs(p, (o - d_c) >> 1, rf, &c, &s);
       const float r0 = a0 * c - a1 * s, r1 = a0 * s + a1 * c;
       a0 = r0;
       a1 = r1;
@@ -131,7 +131,7 @@ struct QueryEp {
   int64_t qc_tok, qc_head, qr_tok, qr_head;  // strides (elements)
   const int32_t* pos;
   int n_h, d_hc, d_hr;
-  float base;
+  RopeFreqs rf;
   __device__ void operator()(int n, int o, float a0, float a1) const {
     const int nc = n_h * d_hc;
     if (o < nc) {
@@ -142,7 +142,7 @@ struct QueryEp {
     } else {
       const int r = o - nc, i = r / d_hr, e = r % d_hr;
       float c, s;
-      rope_cs(pos[n], e >> 1, d_hr, base, &c, &s);
+      rope_cs(pos[n], e >> 1, rf, &c, &s);
       T* dst = q_r + n * qr_tok + i * qr_head + e;
       dst[0] = from_f<T>(a0 * c - a1 * s);
       dst[1] = from_f<T>(a0 * s + a1 * c);
@@ -168,7 +168,7 @@ static mla_status_t append_t(const mla_dims_t* d, const mla_weights_t* w, const 
                              const int32_t* seq_idx, const int32_t* pos, int n,
                              mla_cache_t* cache, cudaStream_t st) {
   AppendEp<T> ep{(T*)cache->rows, (int64_t)(d->d_c + d->d_hr), cache->capacity, cache->seq_base,
-                 seq_idx, pos, d->d_c, d->d_hr, d->rope_base};
+                 seq_idx, pos, d->d_c, rope_freqs(d)};
   launch_linear<T, T>(K_APPEND, (const T*)h, d->d, nullptr, n, (const T*)w->W_DKV, d->d_c,
                       (const T*)w->W_KR, d->d_c + d->d_hr, d->d, ep, st);
   return launch_status();
@@ -198,7 +198,7 @@ static mla_status_t project_q_t(const mla_dims_t* d, const mla_weights_t* w, con
                       (const T*)w->W_DQ, d->d_cq, d->d, StoreF32Ep{cq, d->d_cq}, st);
   QueryEp<T> ep{(T*)q_c, (T*)q_r, (int64_t)d->n_h * d->d_hc, d->d_hc,
                 (int64_t)d->n_h * d->d_hr, d->d_hr, pos, d->n_h, d->d_hc, d->d_hr,
-                d->rope_base};
+                rope_freqs(d)};
   const int nc = d->n_h * d->d_hc, nr = d->n_h * d->d_hr;
   launch_linear<float, T>(K_Q_UP, cq, d->d_cq, nullptr, n, (const T*)w->W_UQ, nc,
                           (const T*)w->W_QR, nc + nr, d->d_cq, ep, st);
@@ -642,7 +642,7 @@ static mla_status_t prefill_t(const mla_dims_t* d, const mla_weights_t* w, const
   // cache rows for every prompt token
   {
     AppendEp<T> ep{(T*)cache->rows, (int64_t)(d->d_c + d->d_hr), cache->capacity,
-                   cache->seq_base, tseq, tpos, d->d_c, d->d_hr, d->rope_base};
+                   cache->seq_base, tseq, tpos, d->d_c, rope_freqs(d)};
     launch_linear<T, T>(K_PREFILL_APPEND, (const T*)h, d->d, nullptr, n, (const T*)w->W_DKV,
                         d->d_c, (const T*)w->W_KR, d->d_c + d->d_hr, d->d, ep, st);
   }
@@ -651,7 +651,7 @@ static mla_status_t prefill_t(const mla_dims_t* d, const mla_weights_t* w, const
                       d->d_cq, (const T*)w->W_DQ, d->d_cq, d->d, StoreF32Ep{cq, d->d_cq}, st);
   {
     QueryEp<float> ep{Q, Q + d->d_hc, (int64_t)d->n_h * dh, dh, (int64_t)d->n_h * dh, dh,
-                      tpos, d->n_h, d->d_hc, d->d_hr, d->rope_base};
+                      tpos, d->n_h, d->d_hc, d->d_hr, rope_freqs(d)};
     const int nc = d->n_h * d->d_hc, nr = d->n_h * d->d_hr;
     launch_linear<float, T>(K_PREFILL_Q_UP, cq, d->d_cq, nullptr, n, (const T*)w->W_UQ, nc,
                             (const T*)w->W_QR, nc + nr, d->d_cq, ep, st);
