@@ -218,6 +218,7 @@ def workload_config(wl):
     return {"workload": wl.name, "B": wl.B, "context": int(max(wl.seq_lens)),
             "cache_rows": wl.n_rows, "dims": "d=5120 n_h=128 d_hc=128 d_hr=64 d_c=512 d_cq=1536",
             "step": "append B new rows + project B queries + absorbed decode",
+            "launch": "CUDA graph of the library calls (e2e: eager calls + H2D/D2H copies)",
             "l2": "flushed between timed steps (256 MB write)"}
 
 
@@ -241,9 +242,11 @@ def setup_decode(wl, dev):
     return step, h_dev, h_host, o_host
 
 
-def time_steps(fn, steps, flush, trace_capacity=0):
+def time_steps(fn, steps, flush, trace_capacity=0, hold_ms=0.0):
     """Run ``steps`` steps, each bracketed by CUDA events on the current stream, with an L2
-    flush before each (outside the events). Returns per-step ms and the kernel trace."""
+    flush before each (outside the events). Returns per-step ms and the kernel trace.
+    ``hold_ms`` > 0 enqueues a sleep kernel of about that length before each step (outside the
+    events) so that the whole step is queued before the GPU reaches it."""
     import torch
     import mla_latent_kv_75_b300 as mla
     st = torch.cuda.current_stream()
@@ -252,8 +255,11 @@ def time_steps(fn, steps, flush, trace_capacity=0):
     trace = mla.KernelTrace(trace_capacity) if trace_capacity else None
     if trace:
         trace.__enter__()
+    cycles = int(hold_ms * 1e-3 * 2.0e9)
     for k in range(steps):
         flush()
+        if cycles:
+            torch.cuda._sleep(cycles)
         evs[k][0].record(st)
         fn()
         evs[k][1].record(st)
@@ -292,12 +298,33 @@ def run_ours(args, rank, world, local_rank):
         flush()
         one_step()
     assert mla.mla_get_device_status() == 0
+
+    # The timed decode step is a CUDA graph of the library's launches (how a decode loop runs in
+    # production: no host work between kernels).
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one_step()
+        for _ in range(max(3, args.warmup)):
+            flush()
+            graph.replay()
+        torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        ms, launches = time_steps(one_step, args.steps, flush, trace_capacity=64 * args.steps)
+        if graph is not None:
+            ms, _ = time_steps(graph.replay, args.steps, flush)
+        else:
+            ms, _ = time_steps(one_step, args.steps, flush)
+        # Per-kernel device times: the same step as eager library calls, each enqueued behind a
+        # sleep kernel so that the host never starves the GPU between launches; CUDA event pairs
+        # around every launch (on its stream) then time the kernels alone.
+        _, launches = time_steps(one_step, args.steps, flush, trace_capacity=64 * args.steps,
+                                 hold_ms=0.5)
     torch.cuda.synchronize()
+    assert mla.mla_get_device_status() == 0
     if world > 1:
         dist.barrier()
     total_ms = sum(ms)
@@ -447,6 +474,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the decode step as eager library calls instead of a CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

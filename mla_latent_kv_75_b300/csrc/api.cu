@@ -192,7 +192,7 @@ mla_status_t mla_prefill_workspace_size(const mla_dims_t* d, int32_t n_tok, int3
                                         int32_t max_T, size_t* bytes) {
   MLA_TRY(check_dims(d));
   if (!bytes || n_tok < 0 || B < 0 || max_T < 0) return MLA_ERR_INVALID_ARG;
-  *bytes = simt_prefill_ws(d, n_tok);
+  *bytes = fast_dims(d) ? tc_prefill_ws(d, n_tok) : simt_prefill_ws(d, n_tok);
   return MLA_OK;
 }
 
@@ -214,6 +214,8 @@ mla_status_t mla_prefill(const mla_dims_t* d, const mla_weights_t* w, const void
   MLA_TRY(mla_prefill_workspace_size(d, n_tok, B, max_T, &need));
   if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
   MLA_TRY(check_ptr(ws));
+  if (fast_dims(d))
+    return tc_prefill(d, w, h, cu_seqlens, B, n_tok, max_T, cache, ws, o, as_stream(stream));
   return simt_prefill(d, w, h, cu_seqlens, B, n_tok, max_T, cache, ws, o, as_stream(stream));
 }
 

@@ -355,24 +355,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(qb + kQBox, &tm_qt, &sh.q_full, 448, b * kHeads);
         tma_load_2d(qb + 2 * kQBox, &tm_qr, &sh.q_full, 0, b * kHeads);
       }
+      // all 48 loads in flight at once: the query rows come from L2 and the load latency,
+      // not the bytes, sets the cost of a segment switch
       const uint4* src = reinterpret_cast<const uint4*>(qt + ((int64_t)b * kHeads + h) * kDC);
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        uint4 v[24];
+      uint4 v[48];
 #pragma unroll
-        for (int k = 0; k < 24; ++k) v[k] = __ldg(src + half * 24 + k);
+      for (int k = 0; k < 48; ++k) v[k] = __ldg(src + k);
 #pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          uint32_t r[32];
+      for (int c = 0; c < 6; ++c) {
+        uint32_t r[32];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            r[4 * k] = v[c * 8 + k].x;
-            r[4 * k + 1] = v[c * 8 + k].y;
-            r[4 * k + 2] = v[c * 8 + k].z;
-            r[4 * k + 3] = v[c * 8 + k].w;
-          }
-          tmem_st32u(lane_base + kColQ + (half * 3 + c) * 32, r);
+        for (int k = 0; k < 8; ++k) {
+          r[4 * k] = v[c * 8 + k].x;
+          r[4 * k + 1] = v[c * 8 + k].y;
+          r[4 * k + 2] = v[c * 8 + k].z;
+          r[4 * k + 3] = v[c * 8 + k].w;
         }
+        tmem_st32u(lane_base + kColQ + c * 32, r);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -501,9 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------------------------------
 // Merge of the partials of one sequence: o~ = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,
 // stored as a hi/lo pair of bf16 (o~ = hi + lo to about 2^-16 relative).
-// grid (B, 8): blockIdx.y picks 64 latent columns; thread = (head, half of those columns).
+// grid (B, 32): blockIdx.y picks 16 latent columns; one thread per head.
 // ------------------------------------------------------------------------------------------
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 128;  // one thread per head
+constexpr int kMergeCols = 16;      // latent columns per thread
 
 __global__ void __launch_bounds__(kMergeThreads)
     decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
@@ -512,8 +512,8 @@ __global__ void __launch_bounds__(kMergeThreads)
                         __nv_bfloat16* __restrict__ ol_hi, __nv_bfloat16* __restrict__ ol_lo) {
   __shared__ long long red[8];
   const int b = blockIdx.x;
-  const int h = threadIdx.x & 127;
-  const int c0 = blockIdx.y * 64 + (threadIdx.x >> 7) * 32;
+  const int h = threadIdx.x;
+  const int c0 = blockIdx.y * kMergeCols;
   long long tot_local = 0, before_local = 0;
   for (int k = threadIdx.x; k < B; k += kMergeThreads) {
     const int n = seq_info(seq_len, seq_base, k, max_len, capacity, false).n;
@@ -523,9 +523,9 @@ __global__ void __launch_bounds__(kMergeThreads)
   const long long T = block_sum<kMergeThreads>(tot_local, red);
   const long long cum = block_sum<kMergeThreads>(before_local, red);
   const int n = seq_info(seq_len, seq_base, b, max_len, capacity, false).n;
-  float acc[32];
+  float acc[kMergeCols];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+  for (int i = 0; i < kMergeCols; ++i) acc[i] = 0.f;
   float inv_l = 0.f;
   if (n > 0) {
     const int p_first = pair_of(cum, T, P), p_last = pair_of(cum + n - 1, T, P);
@@ -535,6 +535,7 @@ __global__ void __launch_bounds__(kMergeThreads)
       if (pair_start(pp, T, P) < pair_start(pp + 1, T, P))
         M = fmaxf(M, part_ml[((int64_t)b + pp) * 256 + h]);
     float lsum = 0.f;
+#pragma unroll 2
     for (int pp = p_first; pp <= p_last; ++pp) {
       if (pair_start(pp, T, P) == pair_start(pp + 1, T, P)) continue;
       const int64_t slot = (int64_t)b + pp;
@@ -542,8 +543,8 @@ __global__ void __launch_bounds__(kMergeThreads)
       lsum += w * part_ml[slot * 256 + 128 + h];
       const float4* src = reinterpret_cast<const float4*>(part_o + (slot * kHeads + h) * kDC + c0);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 v = src[i];
+      for (int i = 0; i < kMergeCols / 4; ++i) {
+        const float4 v = __ldg(src + i);
         acc[4 * i] = fmaf(w, v.x, acc[4 * i]);
         acc[4 * i + 1] = fmaf(w, v.y, acc[4 * i + 1]);
         acc[4 * i + 2] = fmaf(w, v.z, acc[4 * i + 2]);
@@ -554,7 +555,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   }
   const int64_t o = ((int64_t)b * kHeads + h) * kDC + c0;
 #pragma unroll
-  for (int i = 0; i < 32; i += 8) {
+  for (int i = 0; i < kMergeCols; i += 8) {
     uint32_t hw[4], lw[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -677,7 +678,7 @@ mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* 
   // 3. merge the partials of each sequence (o~ = 0 for empty sequences)
   {
     TraceScope ts(K_DECODE_MERGE, st);
-    decode_merge_kernel<<<dim3(B, kDC / 64), kMergeThreads, 0, st>>>(
+    decode_merge_kernel<<<dim3(B, kDC / kMergeCols), kMergeThreads, 0, st>>>(
         part, ml, seq_len, cache->seq_base, max_len > 0 ? cache->capacity : 0, B, max_len,
         pairs, hi, lo);
     s = launch_status();

@@ -5,6 +5,10 @@
 // output tile: warp 0 streams 64-wide K slices of W and X into a shared-memory ring with TMA,
 // warp 1 issues tcgen05.mma, warps 2..5 read the accumulator from TMEM and run the epilogue
 // (RoPE on pairs of adjacent output rows, cache-row scatter, dtype conversion).
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "internal.h"
 #include "proj_tc.h"
 #include "tc.cuh"
@@ -15,16 +19,22 @@ using namespace tc;
 
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kThreads = 192;
 constexpr uint32_t kTileA = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kMaxCluster = 8;          // split-K clusters (portable size)
 
-template <int BN>
+// Shared-memory layout: a ring of stages, each holding one 64-deep K slice of A (16 KB) and of
+// the B operand(s) (BN rows each; two with the hi/lo split input), then the barrier block. The
+// ring is as deep as fits in ~200 KB (at most 8), so that decode-sized GEMMs (BN = 32) keep
+// ~160 KB of weights in flight per SM.
+template <int BN, bool kDual>
 struct ProjSmem {
   static constexpr uint32_t kTileB = BN * 128;
-  static constexpr uint32_t kStage = kTileA + kTileB;
+  static constexpr uint32_t kStage = kTileA + (kDual ? 2 : 1) * kTileB;
+  static constexpr int kStages = (200 * 1024) / kStage < 8 ? (200 * 1024) / kStage : 8;
   static constexpr uint32_t kBars = kStages * kStage;
   static constexpr uint32_t kBytes = kBars + 256;
+  static_assert(kBars >= 128 * BN * 4, "split-K receive buffer must fit in the ring");
 };
 
 // Operand modes of the projection GEMM.
@@ -35,17 +45,29 @@ struct ProjSmem {
 //               i.e. MN-major (loaded as two 64 x 64 boxes per 64-deep K slice).
 enum ProjMode : int { kPlain = 0, kGroupedK = 1, kGroupedMN = 2 };
 
-template <int BN, int kMode, class Ep>
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c,
+                                              float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+// One CTA computes a 128 x BN output tile (C = 1; mt_cta consecutive m-tiles per CTA) or, in a
+// cluster of C CTAs, a 1/C share of the K range of one tile (split-K). Split-K partial tiles are
+// reduced through distributed shared memory: CTA c of the cluster sums rows
+// [c * 128/C, (c+1) * 128/C) of all C partials and runs the epilogue on them.
+template <int BN, int kMode, bool kDual, class Ep>
 __global__ void __launch_bounds__(kThreads, 1)
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0,
                      const __grid_constant__ CUtensorMap tm_w1,
                      const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_x2, int m_tiles0, int O, int N,
-                     int k_chunks, int dual, int mt_group, int mt_cta, Ep ep) {
+                     int k_chunks, int mt_group, int mt_cta, int C, Ep ep) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  using S = ProjSmem<BN>;
+  using S = ProjSmem<BN, kDual>;
+  constexpr int kStages = S::kStages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBars);
   uint64_t* empty = full + kStages;
   uint64_t* done = empty + kStages;
@@ -54,11 +76,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.y * BN;
-  const int m_first = blockIdx.x * mt_cta;
-  const int per_tile = dual ? 2 * k_chunks : k_chunks;
-  const int total_chunks = mt_cta * per_tile;
+  const bool split = C > 1;
+  const int cl = split ? (int)cluster_ctarank() : 0;
+  const int m_first = split ? blockIdx.x / C : blockIdx.x * mt_cta;
+  const int n_mt = split ? 1 : mt_cta;
+  const int kcp = (k_chunks + C - 1) / C;  // K chunks per cluster rank
+  const int kc0 = cl * kcp;
+  const int kc_n = min(k_chunks, kc0 + kcp) - kc0;  // >= 1 (C <= k_chunks)
+  const int total_chunks = n_mt * kc_n;
   uint32_t tmem_cols = 32;  // a power of two >= the accumulator columns
-  while (tmem_cols < (uint32_t)(mt_cta * BN)) tmem_cols <<= 1;
+  while (tmem_cols < (uint32_t)(n_mt * BN)) tmem_cols <<= 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -83,20 +110,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch(&tm_x);
     int issued = 0;
     for (int g = 0; g < total_chunks; ++g) {
-      const int i = g / per_tile, kc = g % per_tile;
+      const int i = g / kc_n, kc = kc0 + g % kc_n;
       const int m_tile = m_first + i;
       const int s = g % kStages, r = g / kStages;
       if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort)) break;
       uint8_t* a = smem + s * S::kStage;
       uint8_t* b = a + kTileA;
       mbar_arrive_expect_tx(&full[s], S::kStage);
-      const int kx = (kc % k_chunks) * 64;
-      const CUtensorMap* xm = (dual && kc >= k_chunks) ? &tm_x2 : &tm_x;
+      const int kx = kc * 64;
       if (kMode == kPlain) {
         const bool from_w1 = m_tile >= m_tiles0;
         tma_load_2d(a, from_w1 ? &tm_w1 : &tm_w0, &full[s], kx,
                     (from_w1 ? m_tile - m_tiles0 : m_tile) * 128);
-        tma_load_2d(b, xm, &full[s], kx, n0);
+        tma_load_2d(b, &tm_x, &full[s], kx, n0);
+        if (kDual) tma_load_2d(b + S::kTileB, &tm_x2, &full[s], kx, n0);
       } else {
         const int grp = m_tile / mt_group;
         if (kMode == kGroupedK) {
@@ -106,7 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(a, &tm_w0, &full[s], col, row);
           tma_load_2d(a + kTileA / 2, &tm_w0, &full[s], col + 64, row);
         }
-        tma_load_3d(b, xm, &full[s], kx, grp, n0);
+        tma_load_3d(b, &tm_x, &full[s], kx, grp, n0);
+        if (kDual) tma_load_3d(b + S::kTileB, &tm_x2, &full[s], kx, grp, n0);
       }
       ++issued;
     }
@@ -120,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             : smem_desc(smem_u32(smem), 16, 1024);
     const uint64_t b0 = smem_desc(smem_u32(smem) + kTileA, 16, 1024);
     for (int g = 0; g < total_chunks; ++g) {
-      const int i = g / per_tile, kc = g % per_tile;
+      const int i = g / kc_n, kc = g % kc_n;
       const int s = g % kStages, r = g / kStages;
       if (!warp_wait(&full[s], r & 1, abort)) break;
       tc_fence_after();
@@ -128,9 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t off = (uint64_t)((s * S::kStage) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t adesc = a0 + off + (uint64_t)((kMode == kGroupedMN ? kk * 2048 : kk * 32) >> 4);
-          mma_ss(tmem + i * BN, adesc, b0 + off + (uint64_t)((kk * 32) >> 4), idesc,
-                 (kc | kk) != 0 ? 1u : 0u);
+          const uint64_t adesc =
+              a0 + off + (uint64_t)((kMode == kGroupedMN ? kk * 2048 : kk * 32) >> 4);
+          const uint64_t bdesc = b0 + off + (uint64_t)((kk * 32) >> 4);
+          mma_ss(tmem + i * BN, adesc, bdesc, idesc, (kc | kk) != 0 ? 1u : 0u);
+          if (kDual)
+            mma_ss(tmem + i * BN, adesc, bdesc + (uint64_t)(S::kTileB >> 4), idesc, 1u);
         }
         mma_commit(&empty[s]);
       }
@@ -138,13 +169,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (elect_one()) mma_commit(done);
     __syncwarp();
-  } else if (warp >= 2) {
+  }
+
+  const int q = warp & 3;  // TMEM lane quarter of an epilogue warp
+  const bool epi = warp >= 2;
+  bool ok = true;
+  if (epi) {
+    ok = warp_wait(done, 0, abort);
+    tc_fence_after();
+  }
+  if (!split) {
     // ---------------- epilogue: TMEM -> registers -> global
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    if (mbar_wait(done, 0, abort)) {
-      tc_fence_after();
+    if (epi && ok) {
 #pragma unroll 1
-      for (int i = 0; i < mt_cta; ++i) {
+      for (int i = 0; i < n_mt; ++i) {
         const int o = (m_first + i) * 128 + q * 32 + lane;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -160,8 +198,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    tc_fence_before();
+  } else {
+    // ---------------- split-K: all-to-all reduction of the partial tiles through DSMEM
+    const int R = 128 / C;  // rows reduced by each CTA of the cluster
+    float* recv = reinterpret_cast<float*>(smem);  // [C][R][BN], the ring is drained
+    __syncthreads();
+    cluster_sync();  // every CTA of the cluster finished its MMAs: all rings are free
+    if (epi && ok) {
+      const int row = q * 32 + lane;
+      const int dst = row / R, rr = row % R;
+      const uint32_t base =
+          mapa_shared(smem_u32(recv + ((size_t)cl * R + rr) * BN), (uint32_t)dst);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_cluster_v4(base + (c + 4 * k) * 4, v[4 * k], v[4 * k + 1], v[4 * k + 2],
+                        v[4 * k + 3]);
+      }
+    }
+    cluster_sync();  // all partial rows have arrived
+    if (epi) {
+      const int ts = threadIdx.x - 64;
+      for (int e = ts; e < (R / 2) * BN; e += 128) {
+        const int pr = e / BN, col = e % BN;
+        float v0 = 0.f, v1 = 0.f;
+        for (int src = 0; src < C; ++src) {
+          v0 += recv[((size_t)src * R + 2 * pr) * BN + col];
+          v1 += recv[((size_t)src * R + 2 * pr + 1) * BN + col];
+        }
+        const int o = m_first * 128 + cl * R + 2 * pr, n = n0 + col;
+        if (n < N && o < O) {
+          ep(o, n, v0, v1);
+          if (o + 1 < O) ep(o + 1, n, v1, v0);
+        }
+      }
+    }
   }
+  if (epi) tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -217,13 +294,6 @@ struct EpStoreF32 {
   __device__ void operator()(int o, int n, float v, float) const { y[(int64_t)n * ld + o] = v; }
 };
 
-struct EpStoreF16 {
-  __half* y;
-  int64_t ld;
-  __device__ void operator()(int o, int n, float v, float) const {
-    y[(int64_t)n * ld + o] = __float2half_rn(v);
-  }
-};
 
 // Query up-projection: rows [0, n_h*d_hc) of [W^UQ; W^QR] are q^C, the rest q^R with RoPE.
 template <typename T>
@@ -256,6 +326,67 @@ bool tmap_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int
   return make_tmap(m, base, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 }
 
+// Opt-in shared memory size for a kernel, set once per (function, device).
+mla_status_t ensure_smem(const void* fn, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({fn, dev})) return MLA_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  done.insert({fn, dev});
+  return MLA_OK;
+}
+
+int sm_count() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
+// Split-K cluster size: the largest power of two <= kMaxCluster that keeps the grid within one
+// wave of the SMs and leaves every cluster rank at least one K chunk.
+int choose_split(int tiles, int k_chunks) {
+  const int sms = sm_count();
+  int c = 1;
+  for (int n = 2; n <= kMaxCluster && tiles * n <= sms; n *= 2) {
+    const int per = (k_chunks + n - 1) / n;
+    if (per * (n - 1) >= k_chunks) break;  // the last rank would get no K chunk
+    c = n;
+  }
+  return c;
+}
+
+template <int BN, int kMode, bool kDual, class Ep>
+mla_status_t launch_kernel(const CUtensorMap& tw0, const CUtensorMap& tw1, const CUtensorMap& tx,
+                           const CUtensorMap& tx2, int m_tiles0, int O, int N, int k_chunks,
+                           int mt_group, int mt_cta, int C, int grid_x, int kid, const Ep& ep,
+                           cudaStream_t st) {
+  const uint32_t smem = ProjSmem<BN, kDual>::kBytes + 1024;
+  auto kern = proj_gemm_kernel<BN, kMode, kDual, Ep>;
+  mla_status_t s = ensure_smem((const void*)kern, (int)smem);
+  if (s != MLA_OK) return s;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_x, ceil_div(N, BN), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  TraceScope ts(kid, st);
+  if (cudaLaunchKernelEx(&cfg, kern, tw0, tw1, tx, tx2, m_tiles0, O, N, k_chunks, mt_group,
+                         mt_cta, C, ep) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
 template <int BN, class Ep>
 mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
   CUtensorMap tw0, tw1, tx, tx2;
@@ -265,14 +396,14 @@ mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
   if (!tmap_rows(&tx, a.X, a.N, a.K, a.ldx, BN)) return MLA_ERR_CUDA;
   if (!tmap_rows(&tx2, a.X2 ? a.X2 : a.X, a.N, a.K, a.ldx, BN)) return MLA_ERR_CUDA;
   const int m_tiles = m0 + (a.W1 ? ceil_div(a.O1, 128) : 0);
-  const uint32_t smem = ProjSmem<BN>::kBytes + 1024;
-  auto kern = proj_gemm_kernel<BN, kPlain, Ep>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  dim3 grid(m_tiles, ceil_div(a.N, BN));
-  TraceScope ts(a.kid, st);
-  kern<<<grid, kThreads, smem, st>>>(tw0, tw1, tx, tx2, m0, a.O0 + (a.W1 ? a.O1 : 0), a.N,
-                                     a.K / 64, a.X2 ? 1 : 0, 1, 1, ep);
-  return launch_status();
+  const int k_chunks = a.K / 64;
+  const int C = choose_split(m_tiles * ceil_div(a.N, BN), k_chunks);
+  const int O = a.O0 + (a.W1 ? a.O1 : 0);
+  if (a.X2)
+    return launch_kernel<BN, kPlain, true>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1, 1, C,
+                                           m_tiles * C, a.kid, ep, st);
+  return launch_kernel<BN, kPlain, false>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1, 1, C,
+                                          m_tiles * C, a.kid, ep, st);
 }
 
 template <class Ep>
@@ -316,14 +447,11 @@ mla_status_t launch_grouped_bn(const GroupArgs& a, const Ep& ep, cudaStream_t st
   int mt_cta = mt_group;
   while (mt_cta * BN > 512 || mt_group % mt_cta) --mt_cta;
   const int m_tiles = a.G * mt_group;
-  const uint32_t smem = ProjSmem<BN>::kBytes + 1024;
-  auto kern = proj_gemm_kernel<BN, kMode, Ep>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  dim3 grid(m_tiles / mt_cta, ceil_div(a.N, BN));
-  TraceScope ts(a.kid, st);
-  kern<<<grid, kThreads, smem, st>>>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, a.K / 64,
-                                     a.X2 ? 1 : 0, mt_group, mt_cta, ep);
-  return launch_status();
+  if (a.X2)
+    return launch_kernel<BN, kMode, true>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, a.K / 64,
+                                          mt_group, mt_cta, 1, m_tiles / mt_cta, a.kid, ep, st);
+  return launch_kernel<BN, kMode, false>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, a.K / 64,
+                                         mt_group, mt_cta, 1, m_tiles / mt_cta, a.kid, ep, st);
 }
 
 template <int kMode, class Ep>
@@ -406,7 +534,7 @@ mla_status_t tc_expand(const void* W, int O, const void* latent, int64_t ld_late
   a.ldx = ld_latent;
   a.N = n;
   a.kid = kid;
-  EpStoreF16 ep{(__half*)y, O};
+  EpStoreBF16 ep{(__nv_bfloat16*)y, nullptr, O};
   return launch_proj(a, ep, st);
 }
 

@@ -61,6 +61,12 @@ mla_status_t tc_absorb(const mla_dims_t* d, const mla_weights_t* w, const void* 
 mla_status_t tc_unabsorb(const mla_dims_t* d, const mla_weights_t* w, const void* ol_hi,
                          const void* ol_lo, int B, float* o, int kid, cudaStream_t st);
 
+// Tensor-core causal prefill (V2 widths, bf16): prefill_tc.cu
+size_t tc_prefill_ws(const mla_dims_t* d, int n_tok);
+mla_status_t tc_prefill(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                        const int32_t* cu, int B, int n, int max_T, mla_cache_t* cache, void* ws,
+                        float* o, cudaStream_t st);
+
 // Tensor-core absorbed decode (V2 widths, bf16): decode_tc.cu
 size_t tc_decode_ws(const mla_dims_t* d, int B);
 mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* q_c,
