@@ -70,6 +70,20 @@ def prefill_flops(wl: mi.Workload):
     return attn, proj + expand
 
 
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu capture, or None when there
+    is none for this workload or the kernel source changed since it was taken."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[kernel]
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+        if rec["workload"] != workload or hashlib.sha1(src).hexdigest() != rec["sha1"]:
+            return None
+        return int(rec["bytes"])
+    except Exception:
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -389,7 +403,7 @@ def run_ours(args, rank, world, local_rank):
                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                         "frac": round(achieved / peaks["bf16_tflops"], 4)}
         roofline["peak_source"] = peaks["source"]
-        roofline["traffic"] = None
+        roofline["traffic"] = measured_traffic(dominant, wl.name)
 
     # the absorbed-decode call alone (absorb + attention + combine)
     dec_names = ("absorb", "decode_attn", "decode_combine", "decode_merge", "unabsorb")
