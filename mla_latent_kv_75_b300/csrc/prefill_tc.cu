@@ -10,12 +10,14 @@
 //   -> c^Q (hi/lo bf16) -> [q^C ; q^R] per head (bf16, RoPE in the epilogue)
 //   -> K^C = W^UK c and V = W^UV c per head (bf16) -> causal attention (this file).
 //
-// Attention kernel: one CTA per (head, 128-query tile, sequence), heaviest query tiles first.
+// Attention kernel: one CTA per (128-query tile, head, sequence). Blocks are dispatched with all
+// query tiles of a head together (heaviest first), so the K/V tiles they share stay in L2.
 // Warp 0 streams the query tile once and then, per 128-key tile, K = [K^C | k^R] (3 boxes) and
 // V (2 boxes) into two 2-deep rings; warp 1 issues S = Q K^T (K = 192) into one of two TMEM
 // score buffers and O += P V with P read from TMEM (the softmax writes P in bf16 over the first
 // 64 columns of the score buffer it came from); warps 2..5 run the online softmax, one thread
-// per query row, in log2 units with lazy rescaling of O.
+// query row and column half (two warps per TMEM lane quarter, 64 key columns each), in log2
+// units with lazy rescaling of O.
 #include "internal.h"
 #include "tc.cuh"
 
@@ -37,8 +39,8 @@ constexpr int kOffQ = 0;                     // 3 boxes
 constexpr int kOffK = 3 * kBox;              // 2 stages x 3 boxes
 constexpr int kOffV = kOffK + 6 * kBox;      // 2 stages x 2 boxes
 constexpr int kOffBar = kOffV + 4 * kBox;    // 13 boxes = 208 KB
-constexpr int kThreads = 192;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
+constexpr int kThreads = 320;  // 10 warps: 0 TMA, 1 MMA, 2..9 softmax (two per TMEM lane quarter)
+constexpr int kSmemBytes = kOffBar + 4096 + 1024;
 constexpr uint32_t kColO = 256;  // O: 128 fp32 columns; score buffers at 0 and 128
 constexpr float kTau = 8.f;      // lazy rescale threshold (log2 units)
 
@@ -46,7 +48,10 @@ struct Bars {
   uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done;
   uint32_t tmem_slot;
   int abort;
+  float row_max[2][2][kBQ];  // [tile parity][column half][row]: partial maxima of the halves
+  float row_sum[2][kBQ];     // [column half][row]: final partial row sums
 };
+static_assert(sizeof(Bars) <= 4096, "barrier block");
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -66,8 +71,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars& sh = *reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort = &sh.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x, b = blockIdx.z;
-  const int qt = gridDim.y - 1 - blockIdx.y;  // heaviest query tiles are dispatched first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest query tiles of a head go first
   const int t0 = cu[b], T = cu[b + 1] - t0;
   if (qt * kBQ >= T) return;
   const int n_kt = qt + 1;  // key tiles 0 .. qt (causal)
@@ -80,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.v_full[s], 1);
       mbar_init(&sh.v_empty[s], 1);
       mbar_init(&sh.s_full[s], 1);
-      mbar_init(&sh.p_full[s], 4);
+      mbar_init(&sh.p_full[s], 8);
     }
     mbar_init(&sh.pv_done, 1);
     sh.abort = 0;
@@ -175,69 +180,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the next score tile for this buffer is queued behind PV(kt), which reads P from it
       if (kt + 2 < n_kt && !issue_s(kt + 2)) break;
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else if (warp >= 2) {
     // ------------------------------------------------------------- softmax warps
     const int q = warp & 3;
-    const int row = q * 32 + lane;  // query row = TMEM lane
-    const int qi = qt * kBQ + row;  // position of this query in its sequence
+    const int half = (warp - 2) >> 2;  // key columns [64 half, 64 half + 64) of a tile
+    const int row = q * 32 + lane;     // query row = TMEM lane
+    const int qi = qt * kBQ + row;     // position of this query in its sequence
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    float m_used = -INFINITY, l_sum = 0.f;
+    float m_used = -INFINITY, l_half = 0.f;
+    // `ok` is warp-uniform; after a failed (timed-out) wait a warp skips all work but still
+    // takes part in every named barrier, so that the other softmax warps never block on it
     bool ok = true;
     for (int kt = 0; kt < n_kt; ++kt) {
       const int s = kt & 1;
-      if (!warp_wait(&sh.s_full[s], (kt >> 1) & 1, abort)) {
-        ok = false;
-        break;
+      float sc[64];
+      if (ok) ok = warp_wait(&sh.s_full[s], (kt >> 1) & 1, abort);
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(lane_base + s * 128 + half * 64, *reinterpret_cast<float(*)[32]>(&sc[0]));
+        tmem_ld32(lane_base + s * 128 + half * 64 + 32, *reinterpret_cast<float(*)[32]>(&sc[32]));
+        tmem_wait_ld();
+        // keys j <= qi inside the sequence: only the diagonal tile and a ragged tail are partial
+        const int kmax = min(qi, T - 1) - kt * kBK - half * 64;  // last allowed column index
+        if (kt == qt || (kt + 1) * kBK > T) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i > kmax) sc[i] = -INFINITY;
+        }
+        float mx[4] = {sc[0], sc[1], sc[2], sc[3]};
+#pragma unroll
+        for (int i = 4; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], sc[i]);
+        sh.row_max[kt & 1][half][row] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       }
-      tc_fence_after();
-      float sc[kBK];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_ld32(lane_base + s * 128 + c * 32, *reinterpret_cast<float(*)[32]>(&sc[c * 32]));
-      tmem_wait_ld();
-      // keys j <= qi and inside the sequence (the diagonal tile is the only partial one)
-      const int kmax = min(qi, T - 1) - kt * kBK;  // last allowed key index in this tile
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int i = 0; i < kBK; ++i)
-        if (i <= kmax) mx[i & 3] = fmaxf(mx[i & 3], sc[i]);
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // the two halves of every row
+      if (!ok) continue;
+      const float mt =
+          fmaxf(sh.row_max[kt & 1][0][row], sh.row_max[kt & 1][1][row]) * scale_log2;
       const bool first = kt == 0;
       const float m_new = first ? mt : (mt > m_used + kTau ? mt : m_used);
       const float alpha = (first || m_new == -INFINITY) ? 0.f : ex2(m_used - m_new);
       const float base = m_new == -INFINITY ? 0.f : m_new;  // rows with no key yet
       m_used = m_new;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t w[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t w[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int i = half * 64 + 2 * k;
-          const float p0 = i <= kmax ? ex2(fmaf(sc[i], scale_log2, -base)) : 0.f;
-          const float p1 = i + 1 <= kmax ? ex2(fmaf(sc[i + 1], scale_log2, -base)) : 0.f;
-          w[k] = pack2(p0, p1);
-          const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
-          ls[k & 3] += __low2float(pb) + __high2float(pb);
-        }
-        tmem_st32u(lane_base + s * 128 + half * 32, w);
+      for (int k = 0; k < 32; ++k) {
+        const float p0 = ex2(fmaf(sc[2 * k], scale_log2, -base));
+        const float p1 = ex2(fmaf(sc[2 * k + 1], scale_log2, -base));
+        w[k] = pack2(p0, p1);
+        ls[k & 3] += p0 + p1;
       }
-      l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+      tmem_st32u(lane_base + s * 128 + half * 32, w);
+      l_half = l_half * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       // O may be rescaled only once the previous PV has completed
-      if (kt > 0 && !warp_wait(&sh.pv_done, (kt - 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
+      if (kt > 0) ok = warp_wait(&sh.pv_done, (kt - 1) & 1, abort);
+      if (!ok) continue;
       if (__any_sync(0xffffffffu, !first && alpha != 1.f)) {
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           float ov[32];
-          tmem_ld32(lane_base + kColO + c * 32, ov);
+          tmem_ld32(lane_base + kColO + half * 64 + c * 32, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) ov[k] *= alpha;
-          tmem_st32(lane_base + kColO + c * 32, ov);
+          tmem_st32(lane_base + kColO + half * 64 + c * 32, ov);
         }
       }
       tmem_wait_st();
@@ -245,14 +252,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.p_full[s]);
     }
+    // row sum = both halves' partial sums (they saw the same sequence of maxima)
+    sh.row_sum[half][row] = l_half;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    const float l_sum = sh.row_sum[0][row] + sh.row_sum[1][row];
     if (ok && warp_wait(&sh.pv_done, (n_kt - 1) & 1, abort)) {
       tc_fence_after();
       const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
-      float4* dst = reinterpret_cast<float4*>(o + ((int64_t)(t0 + qi) * kH + h) * kDV);
+      float4* dst =
+          reinterpret_cast<float4*>(o + ((int64_t)(t0 + qi) * kH + h) * kDV + half * 64);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float ov[32];
-        tmem_ld32(lane_base + kColO + c * 32, ov);
+        tmem_ld32(lane_base + kColO + half * 64 + c * 32, ov);
         tmem_wait_ld();
         if (qi < T) {
 #pragma unroll
@@ -373,7 +385,7 @@ mla_status_t tc_prefill(const mla_dims_t* d, const mla_weights_t* w, const void*
     attr_done[dev] = true;
   }
   const float scale_log2 = softmax_scale(d) * 1.4426950408889634f;
-  dim3 grid(kH, ceil_div(max_T, kBQ), B);
+  dim3 grid(ceil_div(max_T, kBQ), kH, B);
   TraceScope ts(K_PREFILL_ATTN, st);
   prefill_attn_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tkc, tv, tkr, cu, scale_log2, o);
   return launch_status();
