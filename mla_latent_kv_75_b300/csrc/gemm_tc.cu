@@ -246,6 +246,154 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Persistent variant of the plain-mode GEMM for many output tiles (prefill-sized N): one CTA
+// per SM walks tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... (m-tile fastest, so that the
+// CTAs in flight share one activation tile), the TMA ring runs on across tile boundaries, and
+// two TMEM accumulators let the epilogue of one tile overlap the MMAs of the next.
+template <int BN, bool kDual, class Ep>
+__global__ void __launch_bounds__(kThreads, 1)
+    proj_gemm_persistent(const __grid_constant__ CUtensorMap tm_w0,
+                         const __grid_constant__ CUtensorMap tm_w1,
+                         const __grid_constant__ CUtensorMap tm_x,
+                         const __grid_constant__ CUtensorMap tm_x2, int m_tiles0, int m_tiles,
+                         int n_tiles, int O, int N, int k_chunks, Ep ep) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  using S = ProjSmem<BN, kDual>;
+  constexpr int kStages = S::kStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBars);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  constexpr uint32_t kCols = 2 * BN < 32 ? 32 : 2 * BN;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_total = m_tiles * n_tiles;
+  const int my_tiles = blockIdx.x < n_total ? (n_total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    *abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    tma_prefetch(&tm_w0);
+    tma_prefetch(&tm_x);
+    int g = 0, issued = 0;
+    bool ok = true;
+    for (int i = 0; ok && i < my_tiles; ++i) {
+      const int t = blockIdx.x + i * gridDim.x;
+      const int m_tile = t % m_tiles, n0 = (t / m_tiles) * BN;
+      const bool from_w1 = m_tile >= m_tiles0;
+      const int a_row = (from_w1 ? m_tile - m_tiles0 : m_tile) * 128;
+      for (int kc = 0; kc < k_chunks; ++kc, ++g) {
+        const int s = g % kStages, r = g / kStages;
+        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        uint8_t* a = smem + s * S::kStage;
+        uint8_t* b = a + kTileA;
+        mbar_arrive_expect_tx(&full[s], S::kStage);
+        tma_load_2d(a, from_w1 ? &tm_w1 : &tm_w0, &full[s], kc * 64, a_row);
+        tma_load_2d(b, &tm_x, &full[s], kc * 64, n0);
+        if (kDual) tma_load_2d(b + S::kTileB, &tm_x2, &full[s], kc * 64, n0);
+        ++issued;
+      }
+    }
+    for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
+      mbar_wait(&full[k % kStages], (k / kStages) & 1, abort);
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (one elected lane of the converged warp)
+    constexpr uint32_t idesc = idesc_f16(128, BN, 1, 0, 0);
+    const uint64_t a0 = smem_desc(smem_u32(smem), 16, 1024);
+    const uint64_t b0 = smem_desc(smem_u32(smem) + kTileA, 16, 1024);
+    int g = 0;
+    bool ok = true;
+    for (int i = 0; ok && i < my_tiles; ++i) {
+      const int buf = i & 1;
+      // the epilogue has drained this accumulator (passes at once for the first two tiles)
+      if (!warp_wait(&acc_empty[buf], ((i >> 1) & 1) ^ 1, abort)) break;
+      tc_fence_after();
+      for (int kc = 0; kc < k_chunks; ++kc, ++g) {
+        const int s = g % kStages, r = g / kStages;
+        if (!warp_wait(&full[s], r & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t off = (uint64_t)((s * S::kStage) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = a0 + off + (uint64_t)((kk * 32) >> 4);
+            const uint64_t bdesc = b0 + off + (uint64_t)((kk * 32) >> 4);
+            mma_ss(tmem + buf * BN, adesc, bdesc, idesc, (kc | kk) != 0 ? 1u : 0u);
+            if (kDual)
+              mma_ss(tmem + buf * BN, adesc, bdesc + (uint64_t)(S::kTileB >> 4), idesc, 1u);
+          }
+          mma_commit(&empty[s]);
+        }
+        __syncwarp();
+      }
+      if (ok) {
+        if (elect_one()) mma_commit(&acc_full[buf]);
+        __syncwarp();
+      }
+    }
+  } else if (warp >= 2) {
+    // ---------------- epilogue: TMEM -> registers -> global, overlapped with the next tile
+    const int q = warp & 3;
+    for (int i = 0; i < my_tiles; ++i) {
+      const int buf = i & 1;
+      const int t = blockIdx.x + i * gridDim.x;
+      const int m_tile = t % m_tiles, n0 = (t / m_tiles) * BN;
+      if (!warp_wait(&acc_full[buf], (i >> 1) & 1, abort)) break;
+      tc_fence_after();
+      const int o = m_tile * 128 + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float vp = __shfl_xor_sync(0xffffffffu, v[j], 1);
+          const int n = n0 + c + j;
+          if (n < N && o < O) ep(o, n, v[j], vp);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
 // ------------------------------------------------------------------------- epilogues
 // Cache append: rows [0, d_c) of [W^DKV; W^KR] are c^KV, rows [d_c, d_c + d_hr) are k^R,
 // rotated by RoPE at the token's position. Optionally also stored to a packed copy.
@@ -387,6 +535,23 @@ mla_status_t launch_kernel(const CUtensorMap& tw0, const CUtensorMap& tw1, const
   return MLA_OK;
 }
 
+template <int BN, bool kDual, class Ep>
+mla_status_t launch_persistent(const CUtensorMap& tw0, const CUtensorMap& tw1,
+                               const CUtensorMap& tx, const CUtensorMap& tx2, int m_tiles0,
+                               int m_tiles, int O, int N, int k_chunks, int kid, const Ep& ep,
+                               cudaStream_t st) {
+  const uint32_t smem = ProjSmem<BN, kDual>::kBytes + 1024;
+  auto kern = proj_gemm_persistent<BN, kDual, Ep>;
+  mla_status_t s = ensure_smem((const void*)kern, (int)smem);
+  if (s != MLA_OK) return s;
+  const int n_tiles = ceil_div(N, BN);
+  const int grid = min(sm_count(), m_tiles * n_tiles);
+  TraceScope ts(kid, st);
+  kern<<<grid, kThreads, smem, st>>>(tw0, tw1, tx, tx2, m_tiles0, m_tiles, n_tiles, O, N,
+                                     k_chunks, ep);
+  return launch_status();
+}
+
 template <int BN, class Ep>
 mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
   CUtensorMap tw0, tw1, tx, tx2;
@@ -399,6 +564,13 @@ mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
   const int k_chunks = a.K / 64;
   const int C = choose_split(m_tiles * ceil_div(a.N, BN), k_chunks);
   const int O = a.O0 + (a.W1 ? a.O1 : 0);
+  if (m_tiles * ceil_div(a.N, BN) > sm_count()) {
+    if (a.X2)
+      return launch_persistent<BN, true>(tw0, tw1, tx, tx2, m0, m_tiles, O, a.N, k_chunks,
+                                         a.kid, ep, st);
+    return launch_persistent<BN, false>(tw0, tw1, tx, tx2, m0, m_tiles, O, a.N, k_chunks,
+                                        a.kid, ep, st);
+  }
   if (a.X2)
     return launch_kernel<BN, kPlain, true>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1, 1, C,
                                            m_tiles * C, a.kid, ep, st);
@@ -412,7 +584,7 @@ mla_status_t launch_proj(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
   if (a.K % 64 || a.O0 % 128) return MLA_ERR_UNSUPPORTED;
   if (a.N <= 32) return launch_proj_bn<32>(a, ep, st);
   if (a.N <= 64) return launch_proj_bn<64>(a, ep, st);
-  if (a.N <= 128) return launch_proj_bn<128>(a, ep, st);
+  if (a.N <= 128 || a.X2) return launch_proj_bn<128>(a, ep, st);  // hi/lo: 4 ring stages
   return launch_proj_bn<256>(a, ep, st);
 }
 
