@@ -71,7 +71,7 @@ struct Shared {
   uint64_t s_full, s_free, p_full, pv_done, q_full;
   uint32_t tmem_slot;
   int abort;
-  int b0, j0;
+  int b0, j0, nt, nospan;
   long long red[8];
 };
 static_assert(sizeof(Shared) <= 256, "barrier block");
@@ -147,6 +147,20 @@ __device__ __forceinline__ int pair_of(long long t, long long T, int P) {
   return p;
 }
 
+// Work split of the tiles over the P CTA pairs.
+// Whole-sequence mode, used whenever it fits: sequence b gets k_b = min(n_b, max(1,
+// floor(n_b P / T))) pairs, and pair c of them takes tiles [c n_b / k_b, (c+1) n_b / k_b) of
+// that sequence alone; pair p writes slot p. No pair then has to re-load the query halfway.
+// Otherwise (more non-empty sequences than pairs, or the k_b overflow P): pairs take contiguous
+// ranges [p T / P, (p+1) T / P) of the concatenated tile list; each (sequence b, pair p)
+// intersection is a segment writing slot b + p.
+__device__ __forceinline__ int pairs_for(int n, long long T, int P) {
+  if (n <= 0) return 0;
+  long long k = (long long)n * P / T;
+  if (k < 1) k = 1;
+  return (int)(k < n ? k : n);
+}
+
 // Walks the tiles of one pair's range sequence by sequence.
 struct Cursor {
   int b, j;
@@ -207,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh.abort = 0;
     sh.b0 = 0;
     sh.j0 = 0;
+    sh.nt = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -219,32 +234,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch(&tm_qr);
   }
 
-  // ---- plan: total tile count T, this pair's range and its first (sequence, tile)
-  long long local = 0;
-  for (int b = threadIdx.x; b < B; b += kThreads)
-    local += seq_info(seq_len, seq_base, b, max_len, capacity, blockIdx.x == 0).n;
-  const long long T = block_sum<kThreads>(local, sh.red);
-  const long long t_begin = T > 0 ? pair_start(p, T, P) : 0;
-  const long long t_end = T > 0 ? pair_start(p + 1, T, P) : 0;
-  if (t_begin < t_end) {
-    long long carry = 0;
-    for (int b_lo = 0; b_lo < B; b_lo += kThreads) {
-      const int b = b_lo + threadIdx.x;
-      const int n = b < B ? seq_info(seq_len, seq_base, b, max_len, capacity, false).n : 0;
-      long long tot;
-      const long long excl = carry + block_excl_scan<kThreads>(n, sh.red, &tot);
-      if (n > 0 && excl <= t_begin && t_begin < excl + n) {
-        sh.b0 = b;
-        sh.j0 = (int)(t_begin - excl);
+  // ---- plan (see pairs_for): this pair's first (sequence, tile) and tile count
+  long long loc_n = 0, loc_ne = 0;
+  for (int b = threadIdx.x; b < B; b += kThreads) {
+    const int n = seq_info(seq_len, seq_base, b, max_len, capacity, blockIdx.x == 0).n;
+    loc_n += n;
+    loc_ne += n > 0;
+  }
+  const long long T = block_sum<kThreads>(loc_n, sh.red);
+  const long long NE = block_sum<kThreads>(loc_ne, sh.red);
+  long long loc_k = 0;
+  if (T > 0)
+    for (int b = threadIdx.x; b < B; b += kThreads)
+      loc_k += pairs_for(seq_info(seq_len, seq_base, b, max_len, capacity, false).n, T, P);
+  const long long K = block_sum<kThreads>(loc_k, sh.red);
+  const bool nospan = T > 0 && NE <= P && K <= P;
+  if (threadIdx.x == 0) sh.nospan = nospan;
+  if (nospan) {
+    if (p < K) {
+      long long carry = 0;
+      for (int b_lo = 0; b_lo < B; b_lo += kThreads) {
+        const int b = b_lo + threadIdx.x;
+        const int n = b < B ? seq_info(seq_len, seq_base, b, max_len, capacity, false).n : 0;
+        const int k = pairs_for(n, T, P);
+        long long tot;
+        const long long excl = carry + block_excl_scan<kThreads>(k, sh.red, &tot);
+        if (k > 0 && excl <= p && p < excl + k) {
+          const int c = (int)(p - excl);
+          const int j0 = (int)((long long)c * n / k), j1 = (int)((long long)(c + 1) * n / k);
+          sh.b0 = b;
+          sh.j0 = j0;
+          sh.nt = j1 - j0;
+        }
+        carry += tot;
+        if (carry > p) break;
       }
-      carry += tot;
-      if (carry > t_begin) break;
+    }
+  } else if (T > 0) {
+    const long long t_begin = pair_start(p, T, P), t_end = pair_start(p + 1, T, P);
+    if (threadIdx.x == 0) sh.nt = (int)(t_end - t_begin);
+    if (t_begin < t_end) {
+      long long carry = 0;
+      for (int b_lo = 0; b_lo < B; b_lo += kThreads) {
+        const int b = b_lo + threadIdx.x;
+        const int n = b < B ? seq_info(seq_len, seq_base, b, max_len, capacity, false).n : 0;
+        long long tot;
+        const long long excl = carry + block_excl_scan<kThreads>(n, sh.red, &tot);
+        if (n > 0 && excl <= t_begin && t_begin < excl + n) {
+          sh.b0 = b;
+          sh.j0 = (int)(t_begin - excl);
+        }
+        carry += tot;
+        if (carry > t_begin) break;
+      }
     }
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_slot;
-  const int nt = (int)(t_end - t_begin);
+  const int nt = sh.nt;
   uint8_t* const qb = smem + kOffQb;
   uint8_t* const pbuf = smem + kOffP;
 
@@ -466,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!warp_wait(&sh.pv_done, t & 1, abort)) break;
         tc_fence_after();
-        const int64_t slot = (int64_t)b_done + p;
+        const int64_t slot = sh.nospan ? (int64_t)p : (int64_t)b_done + p;
         float4* dst = reinterpret_cast<float4*>(part_o + (slot * kHeads + h) * kDC + rank * 256);
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
@@ -514,31 +562,56 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int b = blockIdx.x;
   const int h = threadIdx.x;
   const int c0 = blockIdx.y * kMergeCols;
-  long long tot_local = 0, before_local = 0;
+  // the work split of the attention kernel (pairs_for), recomputed
+  long long loc_n = 0, loc_ne = 0, loc_before = 0;
   for (int k = threadIdx.x; k < B; k += kMergeThreads) {
     const int n = seq_info(seq_len, seq_base, k, max_len, capacity, false).n;
-    tot_local += n;
-    if (k < b) before_local += n;
+    loc_n += n;
+    loc_ne += n > 0;
+    if (k < b) loc_before += n;
   }
-  const long long T = block_sum<kMergeThreads>(tot_local, red);
-  const long long cum = block_sum<kMergeThreads>(before_local, red);
+  const long long T = block_sum<kMergeThreads>(loc_n, red);
+  const long long NE = block_sum<kMergeThreads>(loc_ne, red);
+  const long long cum = block_sum<kMergeThreads>(loc_before, red);
+  long long loc_k = 0, loc_kb = 0;
+  if (T > 0)
+    for (int k = threadIdx.x; k < B; k += kMergeThreads) {
+      const int kk = pairs_for(seq_info(seq_len, seq_base, k, max_len, capacity, false).n, T, P);
+      loc_k += kk;
+      if (k < b) loc_kb += kk;
+    }
+  const long long K = block_sum<kMergeThreads>(loc_k, red);
+  const long long kcum = block_sum<kMergeThreads>(loc_kb, red);
+  const bool nospan = T > 0 && NE <= P && K <= P;
   const int n = seq_info(seq_len, seq_base, b, max_len, capacity, false).n;
   float acc[kMergeCols];
 #pragma unroll
   for (int i = 0; i < kMergeCols; ++i) acc[i] = 0.f;
   float inv_l = 0.f;
   if (n > 0) {
-    const int p_first = pair_of(cum, T, P), p_last = pair_of(cum + n - 1, T, P);
+    // slots of this sequence's segments: [kcum, kcum + k_b) in whole-sequence mode, else b + p
+    // for the pairs p whose range meets the sequence (pairs with an empty range wrote nothing)
+    int s_first, s_last;
+    if (nospan) {
+      s_first = (int)kcum;
+      s_last = (int)kcum + pairs_for(n, T, P) - 1;
+    } else {
+      s_first = b + pair_of(cum, T, P);
+      s_last = b + pair_of(cum + n - 1, T, P);
+    }
+    auto used = [&](int slot) {
+      if (nospan) return true;
+      const int pp = slot - b;
+      return pair_start(pp, T, P) < pair_start(pp + 1, T, P);
+    };
     float M = -INFINITY;
-    // pairs with an empty range (fewer tiles than pairs) wrote nothing
-    for (int pp = p_first; pp <= p_last; ++pp)
-      if (pair_start(pp, T, P) < pair_start(pp + 1, T, P))
-        M = fmaxf(M, part_ml[((int64_t)b + pp) * 256 + h]);
+    for (int sl = s_first; sl <= s_last; ++sl)
+      if (used(sl)) M = fmaxf(M, part_ml[(int64_t)sl * 256 + h]);
     float lsum = 0.f;
 #pragma unroll 2
-    for (int pp = p_first; pp <= p_last; ++pp) {
-      if (pair_start(pp, T, P) == pair_start(pp + 1, T, P)) continue;
-      const int64_t slot = (int64_t)b + pp;
+    for (int sl = s_first; sl <= s_last; ++sl) {
+      if (!used(sl)) continue;
+      const int64_t slot = sl;
       const float w = exp2f(part_ml[slot * 256 + h] - M);
       lsum += w * part_ml[slot * 256 + 128 + h];
       const float4* src = reinterpret_cast<const float4*>(part_o + (slot * kHeads + h) * kDC + c0);
