@@ -84,8 +84,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kc0 = cl * kcp;
   const int kc_n = min(k_chunks, kc0 + kcp) - kc0;  // >= 1 (C <= k_chunks)
   const int total_chunks = n_mt * kc_n;
+  // With the hi/lo input the two B tiles are adjacent in shared memory and one MMA of width
+  // 2*BN covers both (the weight slice is read once); the epilogue adds the two halves.
+  constexpr int kAccN = kDual ? 2 * BN : BN;  // accumulator columns per output tile
   uint32_t tmem_cols = 32;  // a power of two >= the accumulator columns
-  while (tmem_cols < (uint32_t)(n_mt * BN)) tmem_cols <<= 1;
+  while (tmem_cols < (uint32_t)(n_mt * kAccN)) tmem_cols <<= 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&full[g % kStages], (g / kStages) & 1, abort);
   } else if (warp == 1) {
     // ---------------- MMA issuer (one elected lane of the converged warp)
-    constexpr uint32_t idesc = idesc_f16(128, BN, 1, kMode == kGroupedMN ? 1 : 0, 0);
+    constexpr uint32_t idesc = idesc_f16(128, kAccN, 1, kMode == kGroupedMN ? 1 : 0, 0);
     const uint64_t a0 = kMode == kGroupedMN ? smem_desc(smem_u32(smem), 8192, 1024)
                                             : smem_desc(smem_u32(smem), 16, 1024);
     const uint64_t b0 = smem_desc(smem_u32(smem) + kTileA, 16, 1024);
@@ -159,9 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t adesc =
               a0 + off + (uint64_t)((kMode == kGroupedMN ? kk * 2048 : kk * 32) >> 4);
           const uint64_t bdesc = b0 + off + (uint64_t)((kk * 32) >> 4);
-          mma_ss(tmem + i * BN, adesc, bdesc, idesc, (kc | kk) != 0 ? 1u : 0u);
-          if (kDual)
-            mma_ss(tmem + i * BN, adesc, bdesc + (uint64_t)(S::kTileB >> 4), idesc, 1u);
+          mma_ss(tmem + i * kAccN, adesc, bdesc, idesc, (kc | kk) != 0 ? 1u : 0u);
         }
         mma_commit(&empty[s]);
       }
@@ -187,7 +188,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           float v[32];
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + i * BN + c, v);
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + i * kAccN + c, v);
+          if (kDual) {
+            float v2[32];
+            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + i * kAccN + BN + c, v2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += v2[j];
+          }
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -213,6 +221,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < BN; c += 32) {
         float v[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c, v);
+        if (kDual) {
+          float v2[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + BN + c, v2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += v2[j];
+        }
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -268,7 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  constexpr uint32_t kCols = 2 * BN < 32 ? 32 : 2 * BN;
+  constexpr int kAccN = kDual ? 2 * BN : BN;  // hi/lo: one MMA of width 2*BN (see above)
+  constexpr uint32_t kCols = 2 * kAccN < 32 ? 32 : 2 * kAccN;
+  static_assert(2 * kAccN <= 512, "two accumulators must fit in tensor memory");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_total = m_tiles * n_tiles;
@@ -324,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&full[k % kStages], (k / kStages) & 1, abort);
   } else if (warp == 1) {
     // ---------------- MMA issuer (one elected lane of the converged warp)
-    constexpr uint32_t idesc = idesc_f16(128, BN, 1, 0, 0);
+    constexpr uint32_t idesc = idesc_f16(128, kAccN, 1, 0, 0);
     const uint64_t a0 = smem_desc(smem_u32(smem), 16, 1024);
     const uint64_t b0 = smem_desc(smem_u32(smem) + kTileA, 16, 1024);
     int g = 0;
@@ -347,9 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t adesc = a0 + off + (uint64_t)((kk * 32) >> 4);
             const uint64_t bdesc = b0 + off + (uint64_t)((kk * 32) >> 4);
-            mma_ss(tmem + buf * BN, adesc, bdesc, idesc, (kc | kk) != 0 ? 1u : 0u);
-            if (kDual)
-              mma_ss(tmem + buf * BN, adesc, bdesc + (uint64_t)(S::kTileB >> 4), idesc, 1u);
+            mma_ss(tmem + buf * kAccN, adesc, bdesc, idesc, (kc | kk) != 0 ? 1u : 0u);
           }
           mma_commit(&empty[s]);
         }
@@ -373,7 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + c, v);
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * kAccN + c, v);
+        if (kDual) {
+          float v2[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * kAccN + BN + c, v2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += v2[j];
+        }
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -565,9 +587,13 @@ mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
   const int C = choose_split(m_tiles * ceil_div(a.N, BN), k_chunks);
   const int O = a.O0 + (a.W1 ? a.O1 : 0);
   if (m_tiles * ceil_div(a.N, BN) > sm_count()) {
-    if (a.X2)
-      return launch_persistent<BN, true>(tw0, tw1, tx, tx2, m0, m_tiles, O, a.N, k_chunks,
-                                         a.kid, ep, st);
+    if (a.X2) {
+      if constexpr (BN <= 128)  // two accumulators of width 2*BN must fit in tensor memory
+        return launch_persistent<BN, true>(tw0, tw1, tx, tx2, m0, m_tiles, O, a.N, k_chunks,
+                                           a.kid, ep, st);
+      else
+        return MLA_ERR_UNSUPPORTED;
+    }
     return launch_persistent<BN, false>(tw0, tw1, tx, tx2, m0, m_tiles, O, a.N, k_chunks,
                                         a.kid, ep, st);
   }
@@ -617,7 +643,8 @@ mla_status_t launch_grouped_bn(const GroupArgs& a, const Ep& ep, cudaStream_t st
   if (!map3(&tx, a.X) || !map3(&tx2, a.X2 ? a.X2 : a.X)) return MLA_ERR_CUDA;
   const int mt_group = a.Mg / 128;
   int mt_cta = mt_group;
-  while (mt_cta * BN > 512 || mt_group % mt_cta) --mt_cta;
+  const int acc_n = a.X2 ? 2 * BN : BN;  // accumulator columns per tile (hi/lo: both halves)
+  while (mt_cta * acc_n > 512 || mt_group % mt_cta) --mt_cta;
   const int m_tiles = a.G * mt_group;
   if (a.X2)
     return launch_kernel<BN, kMode, true>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, a.K / 64,
