@@ -98,6 +98,34 @@ def test_v2_decode_on_synthetic_cache_and_queries():
     assert_close(o[1], want[1], "bf16", "length-1 decode")
 
 
+def test_v2_decode_many_short_sequences_spanning_split():
+    """More non-empty sequences than SM pairs: the tensor-core decode then gives each pair a
+    contiguous range of the concatenated tile list, so pairs cross sequence boundaries (query
+    re-load mid-range, one partial slot per segment). Lengths are short and ragged, some below
+    one tile, some exactly at tile multiples; checked on a subset of heads."""
+    dims = mi.V2
+    rng = np.random.default_rng(7)
+    lens = [int(x) for x in rng.integers(1, 200, 150)]
+    lens[3], lens[10], lens[20] = 48, 96, 1
+    W, W64 = oracle_weights(dims, "bf16")
+    model = host.DeviceModel.upload(dims, "bf16", W)
+    base = mi.packed_layout(lens, guard=1)
+    cap = int(base[-1] + lens[-1] + 1)
+    rows_np = mi.aux_normal((cap, dims.row), index=110, dtype="bf16")
+    cache = host.LatentCache(dims, "bf16", base, cap)
+    cache.rows.copy_(host.to_device(rows_np, "bf16"))
+    q_c = mi.aux_normal((len(lens), dims.n_h, dims.d_hc), index=111, dtype="bf16")
+    q_r = mi.aux_normal((len(lens), dims.n_h, dims.d_hr), index=112, dtype="bf16")
+    step = host.DecodeStep(model, cache, lens)
+    o = step.decode(q_c=host.to_device(q_c, "bf16"), q_r=host.to_device(q_r, "bf16"))
+    assert mla.mla_get_device_status() == 0
+    o = o.cpu().numpy()
+    heads = [0, 63, 127]
+    rows = [rows_np[base[b]: base[b] + L].astype(np.float64) for b, L in enumerate(lens)]
+    want = ref.decode_explicit(q_c, q_r, rows, W64["W_UK"], W64["W_UV"], dims.d_c, heads=heads)
+    assert_close(o[:, heads], want, "bf16", "decode o (spanning split)")
+
+
 def test_tiny_f32_prefill():
     dims = mi.TINY
     lens = [33, 1, 70]
