@@ -27,11 +27,12 @@ constexpr int kMaxCluster = 8;          // split-K clusters (portable size)
 // the B operand(s) (BN rows each; two with the hi/lo split input), then the barrier block. The
 // ring is as deep as fits in ~200 KB (at most 8), so that decode-sized GEMMs (BN = 32) keep
 // ~160 KB of weights in flight per SM.
-template <int BN, bool kDual>
+template <int BN, bool kDual, int kMaxStages = 8>
 struct ProjSmem {
   static constexpr uint32_t kTileB = BN * 128;
   static constexpr uint32_t kStage = kTileA + (kDual ? 2 : 1) * kTileB;
-  static constexpr int kStages = (200 * 1024) / kStage < 8 ? (200 * 1024) / kStage : 8;
+  static constexpr int kFit = (200 * 1024) / kStage;
+  static constexpr int kStages = kFit < kMaxStages ? kFit : kMaxStages;
   static constexpr uint32_t kBars = kStages * kStage;
   static constexpr uint32_t kBytes = kBars + 256;
   static_assert(kBars >= 128 * BN * 4, "split-K receive buffer must fit in the ring");
@@ -56,7 +57,7 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
 // cluster of C CTAs, a 1/C share of the K range of one tile (split-K). Split-K partial tiles are
 // reduced through distributed shared memory: CTA c of the cluster sums rows
 // [c * 128/C, (c+1) * 128/C) of all C partials and runs the epilogue on them.
-template <int BN, int kMode, bool kDual, class Ep>
+template <int BN, int kMode, bool kDual, int kMaxStages, class Ep>
 __global__ void __launch_bounds__(kThreads, 1)
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0,
                      const __grid_constant__ CUtensorMap tm_w1,
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  using S = ProjSmem<BN, kDual>;
+  using S = ProjSmem<BN, kDual, kMaxStages>;
   constexpr int kStages = S::kStages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBars);
   uint64_t* empty = full + kStages;
@@ -87,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // With the hi/lo input the two B tiles are adjacent in shared memory and one MMA of width
   // 2*BN covers both (the weight slice is read once); the epilogue adds the two halves.
   constexpr int kAccN = kDual ? 2 * BN : BN;  // accumulator columns per output tile
+  static_assert(kAccN <= 256, "one MMA is at most 256 columns wide");
   uint32_t tmem_cols = 32;  // a power of two >= the accumulator columns
   while (tmem_cols < (uint32_t)(n_mt * kAccN)) tmem_cols <<= 1;
 
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   constexpr int kAccN = kDual ? 2 * BN : BN;  // hi/lo: one MMA of width 2*BN (see above)
   constexpr uint32_t kCols = 2 * kAccN < 32 ? 32 : 2 * kAccN;
-  static_assert(2 * kAccN <= 512, "two accumulators must fit in tensor memory");
+  static_assert(kAccN <= 256, "one MMA is at most 256 columns wide");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_total = m_tiles * n_tiles;
@@ -529,13 +531,13 @@ int choose_split(int tiles, int k_chunks) {
   return c;
 }
 
-template <int BN, int kMode, bool kDual, class Ep>
+template <int BN, int kMode, bool kDual, int kMaxStages = 8, class Ep>
 mla_status_t launch_kernel(const CUtensorMap& tw0, const CUtensorMap& tw1, const CUtensorMap& tx,
                            const CUtensorMap& tx2, int m_tiles0, int O, int N, int k_chunks,
                            int mt_group, int mt_cta, int C, int grid_x, int kid, const Ep& ep,
                            cudaStream_t st) {
-  const uint32_t smem = ProjSmem<BN, kDual>::kBytes + 1024;
-  auto kern = proj_gemm_kernel<BN, kMode, kDual, Ep>;
+  const uint32_t smem = ProjSmem<BN, kDual, kMaxStages>::kBytes + 1024;
+  auto kern = proj_gemm_kernel<BN, kMode, kDual, kMaxStages, Ep>;
   mla_status_t s = ensure_smem((const void*)kern, (int)smem);
   if (s != MLA_OK) return s;
   cudaLaunchConfig_t cfg = {};
@@ -597,9 +599,13 @@ mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
     return launch_persistent<BN, false>(tw0, tw1, tx, tx2, m0, m_tiles, O, a.N, k_chunks,
                                         a.kid, ep, st);
   }
-  if (a.X2)
-    return launch_kernel<BN, kPlain, true>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1, 1, C,
-                                           m_tiles * C, a.kid, ep, st);
+  if (a.X2) {
+    if constexpr (BN <= 128)  // one MMA covers both halves: 2*BN columns, at most 256
+      return launch_kernel<BN, kPlain, true>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1, 1, C,
+                                             m_tiles * C, a.kid, ep, st);
+    else
+      return MLA_ERR_UNSUPPORTED;
+  }
   return launch_kernel<BN, kPlain, false>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1, 1, C,
                                           m_tiles * C, a.kid, ep, st);
 }
@@ -646,10 +652,31 @@ mla_status_t launch_grouped_bn(const GroupArgs& a, const Ep& ep, cudaStream_t st
   const int acc_n = a.X2 ? 2 * BN : BN;  // accumulator columns per tile (hi/lo: both halves)
   while (mt_cta * acc_n > 512 || mt_group % mt_cta) --mt_cta;
   const int m_tiles = a.G * mt_group;
-  if (a.X2)
-    return launch_kernel<BN, kMode, true>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, a.K / 64,
-                                          mt_group, mt_cta, 1, m_tiles / mt_cta, a.kid, ep, st);
-  return launch_kernel<BN, kMode, false>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, a.K / 64,
+  const int k_chunks = a.K / 64;
+  if constexpr (BN == 32) if (!a.X2) {
+    // Decode sizes, single input (the absorb): a 4-deep ring lets two CTAs share an SM, at most
+    // two output tiles per CTA and, with one tile per CTA, split-K clusters over the K range, so
+    // that the grid runs as one wave of short-lived CTAs instead of 128 long ones.
+    const int sms = sm_count();
+    int mtc = mt_group < 2 ? mt_group : 2;
+    while (mt_group % mtc) --mtc;
+    int C = 1;
+    if (mtc == 1)
+      while (2 * C <= kMaxCluster && k_chunks % (2 * C) == 0 && k_chunks / (2 * C) >= 2 &&
+             m_tiles * 2 * C <= 2 * sms)
+        C *= 2;
+    const int grid_x = (m_tiles / mtc) * C;
+    return launch_kernel<BN, kMode, false, 4>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, k_chunks,
+                                              mt_group, mtc, C, grid_x, a.kid, ep, st);
+  }
+  if (a.X2) {
+    if constexpr (BN <= 128)  // one MMA covers both halves: 2*BN columns, at most 256
+      return launch_kernel<BN, kMode, true>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, k_chunks,
+                                            mt_group, mt_cta, 1, m_tiles / mt_cta, a.kid, ep, st);
+    else
+      return MLA_ERR_UNSUPPORTED;
+  }
+  return launch_kernel<BN, kMode, false>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, k_chunks,
                                          mt_group, mt_cta, 1, m_tiles / mt_cta, a.kid, ep, st);
 }
 
@@ -659,7 +686,7 @@ mla_status_t launch_grouped(const GroupArgs& a, const Ep& ep, cudaStream_t st) {
   if (a.K % 64 || a.Mg % 128) return MLA_ERR_UNSUPPORTED;
   if (a.N <= 32) return launch_grouped_bn<32, kMode>(a, ep, st);
   if (a.N <= 64) return launch_grouped_bn<64, kMode>(a, ep, st);
-  if (a.N <= 128) return launch_grouped_bn<128, kMode>(a, ep, st);
+  if (a.N <= 128 || a.X2) return launch_grouped_bn<128, kMode>(a, ep, st);  // hi/lo: N <= 256
   return launch_grouped_bn<256, kMode>(a, ep, st);
 }
 
