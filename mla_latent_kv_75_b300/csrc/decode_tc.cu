@@ -550,18 +550,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // stored as a hi/lo pair of bf16 (o~ = hi + lo to about 2^-16 relative).
 // grid (B, 32): blockIdx.y picks 16 latent columns; one thread per head.
 // ------------------------------------------------------------------------------------------
-constexpr int kMergeThreads = 128;  // one thread per head
-constexpr int kMergeCols = 16;      // latent columns per thread
+// LSE merge. One warp per head, kMergeHeads heads per CTA; lane l owns the latent columns
+// 4l + 128j (j < 4), so every load of a partial row and every store of o~ is one contiguous
+// 512-byte (load) or 256-byte (store) warp access.
+constexpr int kMergeHeads = 8;
+constexpr int kMergeThreads = 32 * kMergeHeads;
+constexpr int kMergeVec = kDC / 128;  // float4 groups per lane
 
 __global__ void __launch_bounds__(kMergeThreads)
     decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                         const int32_t* __restrict__ seq_len, const int64_t* __restrict__ seq_base,
                         int64_t capacity, int B, int max_len, int P,
                         __nv_bfloat16* __restrict__ ol_hi, __nv_bfloat16* __restrict__ ol_lo) {
-  __shared__ long long red[8];
+  __shared__ long long red[kMergeThreads / 32];
   const int b = blockIdx.x;
-  const int h = threadIdx.x;
-  const int c0 = blockIdx.y * kMergeCols;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kMergeHeads + (threadIdx.x >> 5);
   // the work split of the attention kernel (pairs_for), recomputed
   long long loc_n = 0, loc_ne = 0, loc_before = 0;
   for (int k = threadIdx.x; k < B; k += kMergeThreads) {
@@ -584,9 +588,9 @@ __global__ void __launch_bounds__(kMergeThreads)
   const long long kcum = block_sum<kMergeThreads>(loc_kb, red);
   const bool nospan = T > 0 && NE <= P && K <= P;
   const int n = seq_info(seq_len, seq_base, b, max_len, capacity, false).n;
-  float acc[kMergeCols];
+  float4 acc[kMergeVec];
 #pragma unroll
-  for (int i = 0; i < kMergeCols; ++i) acc[i] = 0.f;
+  for (int j = 0; j < kMergeVec; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   float inv_l = 0.f;
   if (n > 0) {
     // slots of this sequence's segments: [kcum, kcum + k_b) in whole-sequence mode, else b + p
@@ -604,43 +608,65 @@ __global__ void __launch_bounds__(kMergeThreads)
       const int pp = slot - b;
       return pair_start(pp, T, P) < pair_start(pp + 1, T, P);
     };
+    // Lane k fetches (m, l) of slot s0 + k, so up to 32 slots cost one round of loads; the
+    // partial rows are then read four slots at a time with all sixteen loads in flight.
     float M = -INFINITY;
-    for (int sl = s_first; sl <= s_last; ++sl)
-      if (used(sl)) M = fmaxf(M, part_ml[(int64_t)sl * 256 + h]);
-    float lsum = 0.f;
-#pragma unroll 2
-    for (int sl = s_first; sl <= s_last; ++sl) {
-      if (!used(sl)) continue;
-      const int64_t slot = sl;
-      const float w = exp2f(part_ml[slot * 256 + h] - M);
-      lsum += w * part_ml[slot * 256 + 128 + h];
-      const float4* src = reinterpret_cast<const float4*>(part_o + (slot * kHeads + h) * kDC + c0);
+    for (int s0 = s_first; s0 <= s_last; s0 += 32) {
+      const int sl = s0 + lane;
+      if (sl <= s_last && used(sl)) M = fmaxf(M, part_ml[(int64_t)sl * 256 + h]);
+    }
 #pragma unroll
-      for (int i = 0; i < kMergeCols / 4; ++i) {
-        const float4 v = __ldg(src + i);
-        acc[4 * i] = fmaf(w, v.x, acc[4 * i]);
-        acc[4 * i + 1] = fmaf(w, v.y, acc[4 * i + 1]);
-        acc[4 * i + 2] = fmaf(w, v.z, acc[4 * i + 2]);
-        acc[4 * i + 3] = fmaf(w, v.w, acc[4 * i + 3]);
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float lsum = 0.f;
+    for (int s0 = s_first; s0 <= s_last; s0 += 32) {
+      const int sl = s0 + lane;
+      float w = 0.f;  // stays 0 for slots past the range and for unused slots (never read)
+      if (sl <= s_last && used(sl)) {
+        w = exp2f(part_ml[(int64_t)sl * 256 + h] - M);
+        lsum += w * part_ml[(int64_t)sl * 256 + 128 + h];
+      }
+      const int cnt = min(32, s_last - s0 + 1);
+      for (int k0 = 0; k0 < cnt; k0 += 4) {  // k0 <= 28: every k below is a lane index
+        float wv[4];
+        float4 v[4][kMergeVec];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          wv[u] = __shfl_sync(0xffffffffu, w, k0 + u);
+          const int64_t row = (int64_t)(s0 + k0 + u) * kHeads + h;
+          const float4* src = reinterpret_cast<const float4*>(part_o + row * kDC) + lane;
+#pragma unroll
+          for (int j = 0; j < kMergeVec; ++j)
+            v[u][j] = wv[u] != 0.f ? __ldg(src + 32 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int j = 0; j < kMergeVec; ++j) {
+            acc[j].x = fmaf(wv[u], v[u][j].x, acc[j].x);
+            acc[j].y = fmaf(wv[u], v[u][j].y, acc[j].y);
+            acc[j].z = fmaf(wv[u], v[u][j].z, acc[j].z);
+            acc[j].w = fmaf(wv[u], v[u][j].w, acc[j].w);
+          }
       }
     }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
     inv_l = lsum > 0.f ? 1.f / lsum : 0.f;
   }
-  const int64_t o = ((int64_t)b * kHeads + h) * kDC + c0;
+  const int64_t o = ((int64_t)b * kHeads + h) * kDC + 4 * lane;
 #pragma unroll
-  for (int i = 0; i < kMergeCols; i += 8) {
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float v0 = acc[i + 2 * k] * inv_l, v1 = acc[i + 2 * k + 1] * inv_l;
-      const __nv_bfloat162 hi = __floats2bfloat162_rn(v0, v1);
-      const __nv_bfloat162 lo =
-          __floats2bfloat162_rn(v0 - __low2float(hi), v1 - __high2float(hi));
-      hw[k] = *reinterpret_cast<const uint32_t*>(&hi);
-      lw[k] = *reinterpret_cast<const uint32_t*>(&lo);
-    }
-    *reinterpret_cast<uint4*>(ol_hi + o + i) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(ol_lo + o + i) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  for (int j = 0; j < kMergeVec; ++j) {
+    const float v0 = acc[j].x * inv_l, v1 = acc[j].y * inv_l;
+    const float v2 = acc[j].z * inv_l, v3 = acc[j].w * inv_l;
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v0, v1);
+    const __nv_bfloat162 h23 = __floats2bfloat162_rn(v2, v3);
+    const __nv_bfloat162 l01 =
+        __floats2bfloat162_rn(v0 - __low2float(h01), v1 - __high2float(h01));
+    const __nv_bfloat162 l23 =
+        __floats2bfloat162_rn(v2 - __low2float(h23), v3 - __high2float(h23));
+    auto bits = [](__nv_bfloat162 x) { return *reinterpret_cast<const uint32_t*>(&x); };
+    *reinterpret_cast<uint2*>(ol_hi + o + 128 * j) = make_uint2(bits(h01), bits(h23));
+    *reinterpret_cast<uint2*>(ol_lo + o + 128 * j) = make_uint2(bits(l01), bits(l23));
   }
 }
 
@@ -751,7 +777,7 @@ mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* 
   // 3. merge the partials of each sequence (o~ = 0 for empty sequences)
   {
     TraceScope ts(K_DECODE_MERGE, st);
-    decode_merge_kernel<<<dim3(B, kDC / kMergeCols), kMergeThreads, 0, st>>>(
+    decode_merge_kernel<<<dim3(B, kHeads / kMergeHeads), kMergeThreads, 0, st>>>(
         part, ml, seq_len, cache->seq_base, max_len > 0 ? cache->capacity : 0, B, max_len,
         pairs, hi, lo);
     s = launch_status();

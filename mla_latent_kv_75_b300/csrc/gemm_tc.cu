@@ -58,7 +58,7 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
 // reduced through distributed shared memory: CTA c of the cluster sums rows
 // [c * 128/C, (c+1) * 128/C) of all C partials and runs the epilogue on them.
 template <int BN, int kMode, bool kDual, int kMaxStages, class Ep>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow ring: 2 CTAs/SM
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0,
                      const __grid_constant__ CUtensorMap tm_w1,
                      const __grid_constant__ CUtensorMap tm_x,
@@ -589,6 +589,17 @@ mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
   const int C = choose_split(m_tiles * ceil_div(a.N, BN), k_chunks);
   const int O = a.O0 + (a.W1 ? a.O1 : 0);
   if (m_tiles * ceil_div(a.N, BN) > sm_count()) {
+    if constexpr (BN == 32)
+      if (m_tiles <= 2 * sm_count()) {
+        // Decode sizes (one token tile, up to two m-tiles per SM): a 4-deep ring lets two CTAs
+        // share an SM, so every m-tile streams its weights at once in a single wave instead of
+        // a persistent CTA walking a second tile after the others have finished.
+        if (a.X2)
+          return launch_kernel<BN, kPlain, true, 4>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1,
+                                                    1, 1, m_tiles, a.kid, ep, st);
+        return launch_kernel<BN, kPlain, false, 4>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1, 1,
+                                                   1, m_tiles, a.kid, ep, st);
+      }
     if (a.X2) {
       if constexpr (BN <= 128)  // two accumulators of width 2*BN must fit in tensor memory
         return launch_persistent<BN, true>(tw0, tw1, tx, tx2, m0, m_tiles, O, a.N, k_chunks,

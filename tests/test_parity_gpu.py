@@ -126,6 +126,31 @@ def test_v2_decode_many_short_sequences_spanning_split():
     assert_close(o[:, heads], want, "bf16", "decode o (spanning split)")
 
 
+def test_v2_decode_one_long_sequence_split_over_every_pair():
+    """One sequence longer than 74 tiles of 48 rows: every SM pair takes a contiguous share of
+    it, so the merge combines 74 partial results (more than one warp's worth of slots, with a
+    ragged last tile). Checked on a subset of heads."""
+    dims = mi.V2
+    lens = [74 * 48 + 1000 + 17]
+    W, W64 = oracle_weights(dims, "bf16")
+    model = host.DeviceModel.upload(dims, "bf16", W)
+    base = mi.packed_layout(lens, guard=2)
+    cap = int(base[-1] + lens[-1] + 2)
+    rows_np = mi.aux_normal((cap, dims.row), index=120, dtype="bf16")
+    cache = host.LatentCache(dims, "bf16", base, cap)
+    cache.rows.copy_(host.to_device(rows_np, "bf16"))
+    q_c = mi.aux_normal((1, dims.n_h, dims.d_hc), index=121, dtype="bf16")
+    q_r = mi.aux_normal((1, dims.n_h, dims.d_hr), index=122, dtype="bf16")
+    step = host.DecodeStep(model, cache, lens)
+    o = step.decode(q_c=host.to_device(q_c, "bf16"), q_r=host.to_device(q_r, "bf16"))
+    assert mla.mla_get_device_status() == 0
+    o = o.cpu().numpy()
+    heads = [0, 1, 64, 127]
+    rows = [rows_np[base[0]: base[0] + lens[0]].astype(np.float64)]
+    want = ref.decode_explicit(q_c, q_r, rows, W64["W_UK"], W64["W_UV"], dims.d_c, heads=heads)
+    assert_close(o[:, heads], want, "bf16", "decode o (one long sequence)")
+
+
 def test_tiny_f32_prefill():
     dims = mi.TINY
     lens = [33, 1, 70]
