@@ -231,6 +231,23 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (the job's time is that of its slowest rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, unit_bytes: int, steps: int, total_ms: float) -> float:
+    """Whole-job GB/s: the bytes that all ranks processed over the slowest rank's time."""
+    return world * unit_bytes * steps / (total_ms * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def metric_name():
     return "MLA decode cache GB/s + TFLOP/s (% roofline) on 1 B300; prefill TFLOP/s"
@@ -362,11 +379,7 @@ def run_ours(args, rank, world, local_rank):
     assert mla.mla_get_device_status() == 0
     if world > 1:
         dist.barrier()
-    total_ms = sum(ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(ms), world, dev)
     clocks = clk.summary()
     ms_step = total_ms / args.steps
 
@@ -374,18 +387,14 @@ def run_ours(args, rank, world, local_rank):
         flush()
         one_e2e()
     e2e_ms, _ = time_steps(one_e2e, args.steps, flush)
-    e2e_total = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
+    e2e_total = max_over_ranks(sum(e2e_ms), world, dev)
 
     costs = decode_kernel_costs(wl)
     e = 2 if wl.dtype == "bf16" else 4
     cache_bytes = wl.n_rows * wl.dims.row * e
     step_flops = sum(c["flops"] for c in costs.values())
-    value = world * cache_bytes * args.steps / (total_ms * 1e-3) / 1e9
-    e2e_value = world * cache_bytes * args.steps / (e2e_total * 1e-3) / 1e9
+    value = job_rate(world, cache_bytes, args.steps, total_ms)
+    e2e_value = job_rate(world, cache_bytes, args.steps, e2e_total)
 
     # per-kernel breakdown from the launch trace
     per = {}
