@@ -23,10 +23,12 @@
 //   softmax one thread per head: online softmax in log2 units with lazy rescaling, P in bf16
 // Both CTAs of a pair therefore hold bitwise identical scores and softmax statistics.
 //
-// Work split: the cache tiles of all sequences form one list (sequence by sequence); pair p of
-// P takes the contiguous range [p*T/P, (p+1)*T/P). Every (sequence b, pair p) intersection is
-// one segment whose partial result goes to slot b + p, which is unique because both ranges are
-// ordered; the merge kernel recomputes the same ranges to find a sequence's slots.
+// Work split (see pairs_for): whenever it fits, every pair works inside one sequence (sequence
+// b gets pairs in proportion to its tile count, each a contiguous share of its tiles, and pair
+// p writes slot p), so no pair re-loads the query halfway. Otherwise the cache tiles of all
+// sequences form one list and pair p of P takes the contiguous range [p*T/P, (p+1)*T/P); every
+// (sequence b, pair p) intersection is a segment writing slot b + p, unique because both ranges
+// are ordered. The merge kernel recomputes the same plan to find a sequence's slots.
 #include <mutex>
 
 #include "internal.h"
