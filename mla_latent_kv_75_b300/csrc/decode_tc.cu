@@ -3,11 +3,11 @@
 // associativity) and "MLA前向计算流程" §三分支计算 ④ (softmax over j = 1..t, scale
 // 1/sqrt(d_h^C + d_h^R)).
 //
-// Four launches:
+// Three launches:
 //   absorb      q~[b,i,:] = (W^UK_i)^T q^C[b,i,:]        grouped tcgen05 GEMM (gemm_tc.cu)
 //   attention   split-KV latent attention, this file     (m, l, O~) partials per segment
-//   merge       log-sum-exp merge of the partials        o~[b,i,:] as a hi/lo bf16 pair
-//   unabsorb    o[b,i,:] = W^UV_i o~[b,i,:]              grouped tcgen05 GEMM (gemm_tc.cu)
+//   unabsorb    log-sum-exp merge of the partials, then  o[b,i,:] = W^UV_i o~[b,i,:]
+//               (tcgen05, this file)
 //
 // Attention kernel. All 128 heads form the M dimension of every MMA. The accumulator
 // O~ (128 heads x 512 latent columns, fp32) would fill a whole SM's tensor memory, so two CTAs
@@ -28,7 +28,10 @@
 // p writes slot p), so no pair re-loads the query halfway. Otherwise the cache tiles of all
 // sequences form one list and pair p of P takes the contiguous range [p*T/P, (p+1)*T/P); every
 // (sequence b, pair p) intersection is a segment writing slot b + p, unique because both ranges
-// are ordered. The merge kernel recomputes the same plan to find a sequence's slots.
+// are ordered. The segments holding a sequence's first and last tile record its slot range for
+// the merge.
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -70,7 +73,7 @@ constexpr float kTau = 8.f;  // lazy rescale threshold (log2 units): p <= 2^8 be
 
 struct Shared {
   uint64_t full[kStages], empty_a[kStages], empty_b[kStages];
-  uint64_t s_full, s_free, p_full, pv_done, q_full;
+  uint64_t s_full, s_free, p_full, pv_done, q_full, mma_done;
   uint32_t tmem_slot;
   int abort;
   int b0, j0, nt, nospan;
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const int32_t* __restrict__ seq_len,
                           const int64_t* __restrict__ seq_base, int64_t capacity, int B,
                           int max_len, float scale_log2, float* __restrict__ part_o,
-                          float* __restrict__ part_ml) {
+                          float* __restrict__ part_ml, int2* __restrict__ seq_slots) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -220,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.p_full, 4);
     mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.q_full, 4);
+    mbar_init(&sh.mma_done, 1);
     sh.abort = 0;
     sh.b0 = 0;
     sh.j0 = 0;
@@ -321,8 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++issued;
       if (t + 1 < nt) cur.next(seq_len, seq_base, max_len, capacity);
     }
+    // every issued copy lands before the CTA may exit (even after an abort)
     for (int t = (issued > kStages ? issued - kStages : 0); t < issued; ++t)
-      mbar_wait(&sh.full[t % kStages], (t / kStages) & 1, abort);
+      mbar_wait_drain(&sh.full[t % kStages], (t / kStages) & 1);
   } else if (nt > 0 && warp == 1) {
     // ------------------------------------------------------------- MMA issuer (one elected
     // lane of a converged warp; the descriptors are precomputed and the K loops unrolled)
@@ -388,6 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (t + 1 < nt) cur.next(seq_len, seq_base, max_len, capacity);
     }
+    // every MMA issued by this CTA completes before its tensor memory is freed
+    if (elect_one()) mma_commit(&sh.mma_done);
+    __syncwarp();
+    mbar_wait_drain(&sh.mma_done, 0);
   } else if (nt > 0 && warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------- softmax warps
     const int q = warp & 3;                 // TMEM lane quarter of this warp
@@ -432,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Cursor cur{sh.b0, sh.j0, seq_info(seq_len, seq_base, sh.b0, max_len, capacity, false)};
     load_q(cur.b);
     float m_used = -INFINITY, l_sum = 0.f;
+    int seg_j0 = cur.j;  // first tile of the current segment
     for (int t = 0; t < nt; ++t) {
       const int j = cur.j;
       const int valid = min(kTile, cur.s.L - j * kTile);
@@ -509,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j + 1 == cur.s.n || t + 1 == nt) {
         // end of a segment (end of the sequence or of this pair's range): the next
         // sequence's query first, then O_r and (m, l) to the segment's partial slot
-        const int b_done = cur.b;
+        const int b_done = cur.b, n_done = cur.s.n;
         if (t + 1 < nt) {
           cur.next(seq_len, seq_base, max_len, capacity);
           load_q(cur.b);
@@ -530,7 +540,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rank == 0) {
           part_ml[slot * 256 + h] = m_used;
           part_ml[slot * 256 + 128 + h] = l_sum;
+          // the segments holding a sequence's first and last tile record its slot range
+          if (ts == 0) {
+            if (seg_j0 == 0) seq_slots[b_done].x = (int)slot;
+            if (j + 1 == n_done) seq_slots[b_done].y = (int)slot;
+          }
         }
+        seg_j0 = 0;
         tc_fence_before();
         m_used = -INFINITY;
         l_sum = 0.f;
@@ -548,127 +564,261 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------------------
-// Merge of the partials of one sequence: o~ = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p,
-// stored as a hi/lo pair of bf16 (o~ = hi + lo to about 2^-16 relative).
-// grid (B, 32): blockIdx.y picks 16 latent columns; one thread per head.
+// Merge + un-absorb: o[b,i,:] = W^UV_i o~[b,i,:], with o~ the log-sum-exp merge of the
+// sequence's partial results, o~ = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s (m in log2
+// units). One CTA per (head i, 64 sequences), 16 warps:
+//   - the head's [128 x 512] block of W^UV streams through a 4-deep ring of 64-column chunks
+//     (TMA): thread 0 loads the first four while the partials are merged, warp 8 the rest as
+//     the MMAs free the ring;
+//   - the warps merge the partials in teams: with n sequences in the CTA, G = 16 / n warps (a
+//     power of two, at least 1) share a sequence, each taking every G-th slot of its range and
+//     keeping an online (max, sum, O) in registers, four slots' loads in flight at a time; a
+//     team combines its members through shared memory. Lane l owns latent columns 4l + 128j
+//     (j < 4), so each partial row is one contiguous 512-byte warp load;
+//   - o~ is written as a hi/lo pair of bf16 (o~ = hi + lo to about 2^-16) straight into the
+//     K-major, 128-byte-swizzled B operand: rows 0..63 hold hi, rows 64..127 lo;
+//   - one thread issues D[128 features x 128] = W^UV_i [hi ; lo]^T (32 K-steps of 16);
+//   - eight warps add the two halves of each column and store o (one feature per lane).
+// The slot range of sequence b, [seq_slots[b].x, seq_slots[b].y], was recorded by the attention
+// kernel; every slot in it holds a segment of b.
 // ------------------------------------------------------------------------------------------
-// LSE merge. One warp per head, kMergeHeads heads per CTA; lane l owns the latent columns
-// 4l + 128j (j < 4), so every load of a partial row and every store of o~ is one contiguous
-// 512-byte (load) or 256-byte (store) warp access.
-constexpr int kMergeHeads = 8;
-constexpr int kMergeThreads = 32 * kMergeHeads;
-constexpr int kMergeVec = kDC / 128;  // float4 groups per lane
+constexpr int kUnBN = 64;                              // sequences per CTA
+constexpr int kUnWarps = 16;
+constexpr int kUnThreads = 32 * kUnWarps;
+constexpr int kUnABox = 128 * 128;                     // 128 rows x 64 bf16: one K chunk of A
+constexpr int kUnAStages = 4;
+constexpr int kUnBChunk = 2 * kUnBN * 128;             // one 64-wide K chunk of [hi ; lo]
+constexpr int kUnOffB = kUnAStages * kUnABox;          // A ring: 64 KB
+constexpr int kUnOffTeam = kUnOffB + 8 * kUnBChunk;    // B: 128 KB
+constexpr int kUnTeamFloats = 4 * 128 + 4;             // per warp: O (512), max, sum (16 B rows)
+constexpr int kUnOffBar = kUnOffTeam + kUnWarps * kUnTeamFloats * 4;
+constexpr int kUnSmem = kUnOffBar + 128 + 1024;
+constexpr int kMergeVec = kDC / 128;                   // float4 groups per lane
+static_assert(kUnOffB % 1024 == 0 && kUnOffTeam % 16 == 0 && kUnTeamFloats % 4 == 0, "alignment");
+static_assert(kUnSmem <= 232448, "shared memory");
 
-__global__ void __launch_bounds__(kMergeThreads)
-    decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                        const int32_t* __restrict__ seq_len, const int64_t* __restrict__ seq_base,
-                        int64_t capacity, int B, int max_len, int P,
-                        __nv_bfloat16* __restrict__ ol_hi, __nv_bfloat16* __restrict__ ol_lo) {
-  __shared__ long long red[kMergeThreads / 32];
-  const int b = blockIdx.x;
-  const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y * kMergeHeads + (threadIdx.x >> 5);
-  // the work split of the attention kernel (pairs_for), recomputed
-  long long loc_n = 0, loc_ne = 0, loc_before = 0;
-  for (int k = threadIdx.x; k < B; k += kMergeThreads) {
-    const int n = seq_info(seq_len, seq_base, k, max_len, capacity, false).n;
-    loc_n += n;
-    loc_ne += n > 0;
-    if (k < b) loc_before += n;
+__global__ void __launch_bounds__(kUnThreads, 1)
+    decode_unabsorb_kernel(const __grid_constant__ CUtensorMap tm_wuv,  // W^UV [n_h*128, 512]
+                           const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                           const int2* __restrict__ seq_slots, int n_slots,
+                           const int32_t* __restrict__ seq_len,
+                           const int64_t* __restrict__ seq_base, int64_t capacity, int B,
+                           int max_len, float* __restrict__ o) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + kUnOffBar);
+  uint64_t* a_empty = a_full + kUnAStages;
+  uint64_t* done = a_empty + kUnAStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* team = reinterpret_cast<float*>(smem + kUnOffTeam);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x;  // head
+  const int b0 = blockIdx.y * kUnBN;
+  const int nb = min(kUnBN, B - b0);
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kUnAStages; ++k) {
+      mbar_init(&a_full[k], 1);
+      mbar_init(&a_empty[k], 1);
+    }
+    mbar_init(done, 1);
+    *abort = 0;
+    fence_barrier_init();
   }
-  const long long T = block_sum<kMergeThreads>(loc_n, red);
-  const long long NE = block_sum<kMergeThreads>(loc_ne, red);
-  const long long cum = block_sum<kMergeThreads>(loc_before, red);
-  long long loc_k = 0, loc_kb = 0;
-  if (T > 0)
-    for (int k = threadIdx.x; k < B; k += kMergeThreads) {
-      const int kk = pairs_for(seq_info(seq_len, seq_base, k, max_len, capacity, false).n, T, P);
-      loc_k += kk;
-      if (k < b) loc_kb += kk;
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) {
+    tma_prefetch(&tm_wuv);
+    for (int k = 0; k < kUnAStages; ++k) {
+      mbar_arrive_expect_tx(&a_full[k], kUnABox);
+      tma_load_2d(smem + k * kUnABox, &tm_wuv, &a_full[k], k * 64, i * 128);
     }
-  const long long K = block_sum<kMergeThreads>(loc_k, red);
-  const long long kcum = block_sum<kMergeThreads>(loc_kb, red);
-  const bool nospan = T > 0 && NE <= P && K <= P;
-  const int n = seq_info(seq_len, seq_base, b, max_len, capacity, false).n;
-  float4 acc[kMergeVec];
+  }
+
+  // ---- merge in teams of G warps per sequence
+  int G = 1;
+  while (G * 2 * nb <= kUnWarps) G *= 2;
+  const int teams = kUnWarps / G, g = warp % G;
+  const int rounds = (nb + teams - 1) / teams;
+  auto bits = [](__nv_bfloat162 x) { return *reinterpret_cast<const uint32_t*>(&x); };
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int r = rd * teams + warp / G;  // sequence within the CTA
+    float4 acc[kMergeVec];
 #pragma unroll
-  for (int j = 0; j < kMergeVec; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float inv_l = 0.f;
-  if (n > 0) {
-    // slots of this sequence's segments: [kcum, kcum + k_b) in whole-sequence mode, else b + p
-    // for the pairs p whose range meets the sequence (pairs with an empty range wrote nothing)
-    int s_first, s_last;
-    if (nospan) {
-      s_first = (int)kcum;
-      s_last = (int)kcum + pairs_for(n, T, P) - 1;
-    } else {
-      s_first = b + pair_of(cum, T, P);
-      s_last = b + pair_of(cum + n - 1, T, P);
-    }
-    auto used = [&](int slot) {
-      if (nospan) return true;
-      const int pp = slot - b;
-      return pair_start(pp, T, P) < pair_start(pp + 1, T, P);
-    };
-    // Lane k fetches (m, l) of slot s0 + k, so up to 32 slots cost one round of loads; the
-    // partial rows are then read four slots at a time with all sixteen loads in flight.
-    float M = -INFINITY;
-    for (int s0 = s_first; s0 <= s_last; s0 += 32) {
-      const int sl = s0 + lane;
-      if (sl <= s_last && used(sl)) M = fmaxf(M, part_ml[(int64_t)sl * 256 + h]);
-    }
+    for (int j = 0; j < kMergeVec; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = -INFINITY, L = 0.f;
+    if (r < nb && seq_info(seq_len, seq_base, b0 + r, max_len, capacity, false).n > 0) {
+      const int2 rg = seq_slots[b0 + r];
+      if (rg.x < 0 || rg.y < rg.x || rg.y >= n_slots) {
+        if (lane == 0) flag_status(MLA_ERR_UNSUPPORTED);  // not written by the attention kernel
+      } else {
+        // slots rg.x + g, rg.x + g + G, ...: four at a time, all their loads in flight
+        for (int s0 = rg.x + g; s0 <= rg.y; s0 += 4 * G) {
+          float mv[4], lv[4];
+          float4 v[4][kMergeVec];
 #pragma unroll
-    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float lsum = 0.f;
-    for (int s0 = s_first; s0 <= s_last; s0 += 32) {
-      const int sl = s0 + lane;
-      float w = 0.f;  // stays 0 for slots past the range and for unused slots (never read)
-      if (sl <= s_last && used(sl)) {
-        w = exp2f(part_ml[(int64_t)sl * 256 + h] - M);
-        lsum += w * part_ml[(int64_t)sl * 256 + 128 + h];
-      }
-      const int cnt = min(32, s_last - s0 + 1);
-      for (int k0 = 0; k0 < cnt; k0 += 4) {  // k0 <= 28: every k below is a lane index
-        float wv[4];
-        float4 v[4][kMergeVec];
+          for (int u = 0; u < 4; ++u) {
+            const int sl = s0 + u * G;
+            mv[u] = -INFINITY;
+            lv[u] = 0.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          wv[u] = __shfl_sync(0xffffffffu, w, k0 + u);
-          const int64_t row = (int64_t)(s0 + k0 + u) * kHeads + h;
-          const float4* src = reinterpret_cast<const float4*>(part_o + row * kDC) + lane;
+            for (int j = 0; j < kMergeVec; ++j) v[u][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (sl <= rg.y) {
+              mv[u] = __ldg(part_ml + (int64_t)sl * 256 + i);
+              lv[u] = __ldg(part_ml + (int64_t)sl * 256 + 128 + i);
+              const float4* src =
+                  reinterpret_cast<const float4*>(part_o + ((int64_t)sl * kHeads + i) * kDC) + lane;
 #pragma unroll
-          for (int j = 0; j < kMergeVec; ++j)
-            v[u][j] = wv[u] != 0.f ? __ldg(src + 32 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
+              for (int j = 0; j < kMergeVec; ++j) v[u][j] = __ldg(src + 32 * j);
+            }
+          }
+          const float mx = fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3]));
+          const float Mn = fmaxf(M, mx);
+          const float sc = M == -INFINITY ? 0.f : exp2f(M - Mn);
+          L *= sc;
 #pragma unroll
           for (int j = 0; j < kMergeVec; ++j) {
-            acc[j].x = fmaf(wv[u], v[u][j].x, acc[j].x);
-            acc[j].y = fmaf(wv[u], v[u][j].y, acc[j].y);
-            acc[j].z = fmaf(wv[u], v[u][j].z, acc[j].z);
-            acc[j].w = fmaf(wv[u], v[u][j].w, acc[j].w);
+            acc[j].x *= sc;
+            acc[j].y *= sc;
+            acc[j].z *= sc;
+            acc[j].w *= sc;
           }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float w = mv[u] == -INFINITY ? 0.f : exp2f(mv[u] - Mn);
+            L = fmaf(w, lv[u], L);
+#pragma unroll
+            for (int j = 0; j < kMergeVec; ++j) {
+              acc[j].x = fmaf(w, v[u][j].x, acc[j].x);
+              acc[j].y = fmaf(w, v[u][j].y, acc[j].y);
+              acc[j].z = fmaf(w, v[u][j].z, acc[j].z);
+              acc[j].w = fmaf(w, v[u][j].w, acc[j].w);
+            }
+          }
+          M = Mn;
+        }
       }
     }
+    if (G > 1) {
+      // team members hand (M, L, O) to the team's first warp through shared memory
+      float* mine = team + warp * kUnTeamFloats;
 #pragma unroll
-    for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    inv_l = lsum > 0.f ? 1.f / lsum : 0.f;
+      for (int j = 0; j < kMergeVec; ++j)
+        *reinterpret_cast<float4*>(mine + 4 * lane + 128 * j) = acc[j];
+      if (lane == 0) {
+        mine[512] = M;
+        mine[513] = L;
+      }
+      __syncthreads();
+      if (g == 0) {
+        float Mt = -INFINITY;
+        for (int k = 0; k < G; ++k) Mt = fmaxf(Mt, team[(warp + k) * kUnTeamFloats + 512]);
+#pragma unroll
+        for (int j = 0; j < kMergeVec; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        L = 0.f;
+        for (int k = 0; k < G; ++k) {
+          const float* t = team + (warp + k) * kUnTeamFloats;
+          const float w = t[512] == -INFINITY ? 0.f : exp2f(t[512] - Mt);
+          L = fmaf(w, t[513], L);
+#pragma unroll
+          for (int j = 0; j < kMergeVec; ++j) {
+            const float4 x = *reinterpret_cast<const float4*>(t + 4 * lane + 128 * j);
+            acc[j].x = fmaf(w, x.x, acc[j].x);
+            acc[j].y = fmaf(w, x.y, acc[j].y);
+            acc[j].z = fmaf(w, x.z, acc[j].z);
+            acc[j].w = fmaf(w, x.w, acc[j].w);
+          }
+        }
+      }
+    }
+    if (g == 0 && r < kUnBN) {
+      // o~ -> hi/lo bf16 rows r and 64 + r of the B operand. Columns 4l + 128j sit in K chunk
+      // 2j + l/16, 16-byte unit (l % 16) / 2 (swizzled by the row), half l % 2.
+      const float inv_l = L > 0.f ? 1.f / L : 0.f;
+      const uint32_t unit = (uint32_t)((lane & 15) >> 1);
+      const uint32_t sw = ((unit ^ (uint32_t)(r & 7)) << 4) + (lane & 1) * 8;  // (64 + r) & 7 == r & 7
+#pragma unroll
+      for (int j = 0; j < kMergeVec; ++j) {
+        const float v0 = acc[j].x * inv_l, v1 = acc[j].y * inv_l;
+        const float v2 = acc[j].z * inv_l, v3 = acc[j].w * inv_l;
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(v0, v1);
+        const __nv_bfloat162 h23 = __floats2bfloat162_rn(v2, v3);
+        const __nv_bfloat162 l01 =
+            __floats2bfloat162_rn(v0 - __low2float(h01), v1 - __high2float(h01));
+        const __nv_bfloat162 l23 =
+            __floats2bfloat162_rn(v2 - __low2float(h23), v3 - __high2float(h23));
+        uint8_t* chunk = smem + kUnOffB + (2 * j + (lane >> 4)) * kUnBChunk;
+        *reinterpret_cast<uint2*>(chunk + r * 128 + sw) = make_uint2(bits(h01), bits(h23));
+        *reinterpret_cast<uint2*>(chunk + (kUnBN + r) * 128 + sw) =
+            make_uint2(bits(l01), bits(l23));
+      }
+    }
+    if (G > 1) __syncthreads();  // the team buffer is reused by the next round
   }
-  const int64_t o = ((int64_t)b * kHeads + h) * kDC + 4 * lane;
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  // ---- D[f, n] = sum_k W^UV_i[f, k] B[n, k]: 8 chunks x 4 K-steps; chunks 4..7 of A are
+  // loaded into the ring as the first four are consumed
+  if (warp == 0) {
+    bool ok = true;
+    for (int kc = 0; kc < 8 && ok; ++kc) {
+      ok = warp_wait(&a_full[kc % kUnAStages], (kc / kUnAStages) & 1, abort);
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        constexpr uint32_t idesc = idesc_f16(128, 2 * kUnBN, 1, 0, 0);
+        const uint64_t ad = smem_desc(smem_u32(smem + (kc % kUnAStages) * kUnABox), 16, 1024);
+        const uint64_t bd = smem_desc(smem_u32(smem + kUnOffB + kc * kUnBChunk), 16, 1024);
 #pragma unroll
-  for (int j = 0; j < kMergeVec; ++j) {
-    const float v0 = acc[j].x * inv_l, v1 = acc[j].y * inv_l;
-    const float v2 = acc[j].z * inv_l, v3 = acc[j].w * inv_l;
-    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v0, v1);
-    const __nv_bfloat162 h23 = __floats2bfloat162_rn(v2, v3);
-    const __nv_bfloat162 l01 =
-        __floats2bfloat162_rn(v0 - __low2float(h01), v1 - __high2float(h01));
-    const __nv_bfloat162 l23 =
-        __floats2bfloat162_rn(v2 - __low2float(h23), v3 - __high2float(h23));
-    auto bits = [](__nv_bfloat162 x) { return *reinterpret_cast<const uint32_t*>(&x); };
-    *reinterpret_cast<uint2*>(ol_hi + o + 128 * j) = make_uint2(bits(h01), bits(h23));
-    *reinterpret_cast<uint2*>(ol_lo + o + 128 * j) = make_uint2(bits(l01), bits(l23));
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tmem, ad + (uint64_t)((kk * 32) >> 4), bd + (uint64_t)((kk * 32) >> 4), idesc,
+                 (kc | kk) != 0 ? 1u : 0u);
+        mma_commit(&a_empty[kc % kUnAStages]);
+      }
+      __syncwarp();
+    }
+    if (elect_one()) mma_commit(done);
+    __syncwarp();
+  } else if (warp == 8 && lane == 0) {  // not an epilogue warp
+    int issued = kUnAStages;
+    for (int kc = kUnAStages; kc < 8; ++kc) {
+      if (!mbar_wait(&a_empty[kc % kUnAStages], 0, abort)) break;
+      mbar_arrive_expect_tx(&a_full[kc % kUnAStages], kUnABox);
+      tma_load_2d(smem + (kc % kUnAStages) * kUnABox, &tm_wuv, &a_full[kc % kUnAStages], kc * 64,
+                  i * 128);
+      ++issued;
+    }
+    // every issued copy lands before the CTA may exit (even after an abort)
+    for (int kc = issued - kUnAStages; kc < issued; ++kc)
+      mbar_wait_drain(&a_full[kc % kUnAStages], (kc / kUnAStages) & 1);
+  }
+  // ---- epilogue: lane = output feature; warp w reads columns [32 (w/4), +32) of hi and lo
+  if (warp < 8 && warp_wait(done, 0, abort)) {
+    tc_fence_after();
+    const int c0 = (warp >> 2) * 32;
+    float hi[32], lo[32];
+    tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + c0, hi);
+    tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + kUnBN + c0, lo);
+    tmem_wait_ld();
+    const int f = (warp & 3) * 32 + lane;
+#pragma unroll
+    for (int r = 0; r < 32; ++r)
+      if (c0 + r < nb) o[((int64_t)(b0 + c0 + r) * kHeads + i) * 128 + f] = hi[r] + lo[r];
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    mbar_wait_drain(done, 0);  // the MMAs have completed before tensor memory is freed
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
   }
 }
 
@@ -676,18 +826,17 @@ __global__ void __launch_bounds__(kMergeThreads)
 // Host side
 // ------------------------------------------------------------------------------------------
 struct Layout {
-  size_t off_qt, off_hi, off_lo, off_part, off_ml, total;
+  size_t off_qt, off_part, off_ml, off_rng, total;
 };
 
 Layout layout(int B) {
   Layout L;
   const size_t slots = (size_t)B + kMaxPairs;
   L.off_qt = 0;
-  L.off_hi = align_up(L.off_qt + (size_t)B * kHeads * kDC * 2, 256);
-  L.off_lo = align_up(L.off_hi + (size_t)B * kHeads * kDC * 2, 256);
-  L.off_part = align_up(L.off_lo + (size_t)B * kHeads * kDC * 2, 256);
+  L.off_part = align_up(L.off_qt + (size_t)B * kHeads * kDC * 2, 256);
   L.off_ml = align_up(L.off_part + slots * kDC * kHeads * 4, 256);
-  L.total = align_up(L.off_ml + slots * 256 * 4, 256);
+  L.off_rng = align_up(L.off_ml + slots * 256 * 4, 256);
+  L.total = align_up(L.off_rng + (size_t)B * sizeof(int2), 256);
   return L;
 }
 
@@ -712,11 +861,31 @@ mla_status_t attn_pairs(int* out) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         per_sm < 1)
       return MLA_ERR_CUDA;
-    const int n = per_sm * sms / 2;
+    int n = per_sm * sms / 2;
     if (n < 1) return MLA_ERR_UNSUPPORTED;
-    g_pairs[dev] = n < kMaxPairs ? n : kMaxPairs;
+    if (n > kMaxPairs) n = kMaxPairs;
+    // MLA_DECODE_PAIRS (read once per device) lowers the pair count, for tests and tuning
+    const char* e = getenv("MLA_DECODE_PAIRS");
+    if (e && atoi(e) >= 1 && atoi(e) < n) n = atoi(e);
+    g_pairs[dev] = n;
   }
   *out = g_pairs[dev];
+  return MLA_OK;
+}
+
+// Opt-in shared memory of the merge + un-absorb kernel, set once per device.
+mla_status_t unabsorb_setup() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+  static bool done[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(decode_unabsorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kUnSmem) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    done[dev] = true;
+  }
   return MLA_OK;
 }
 
@@ -730,10 +899,9 @@ mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* 
   const Layout L = layout(B);
   char* wsb = (char*)ws;
   __nv_bfloat16* qt = (__nv_bfloat16*)(wsb + L.off_qt);
-  __nv_bfloat16* hi = (__nv_bfloat16*)(wsb + L.off_hi);
-  __nv_bfloat16* lo = (__nv_bfloat16*)(wsb + L.off_lo);
   float* part = (float*)(wsb + L.off_part);
   float* ml = (float*)(wsb + L.off_ml);
+  int2* rng = (int2*)(wsb + L.off_rng);
   int pairs = 0;
   mla_status_t s = attn_pairs(&pairs);
   if (s != MLA_OK) return s;
@@ -771,23 +939,27 @@ mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* 
     TraceScope ts(K_DECODE_ATTN, st);
     decode_attn_tc_kernel<<<2 * pairs, kThreads, kSmemBytes, st>>>(
         tm_rows, tm_qt, tm_qr, (const __nv_bfloat16*)qt, seq_len, cache->seq_base,
-        cache->capacity, B, max_len, scale_log2, part, ml);
+        cache->capacity, B, max_len, scale_log2, part, ml, rng);
     s = launch_status();
     if (s != MLA_OK) return s;
   }
 
-  // 3. merge the partials of each sequence (o~ = 0 for empty sequences)
+  // 3. merge the partials of each sequence and apply W^UV_i (o = 0 for empty sequences)
+  CUtensorMap tm_wuv;
   {
-    TraceScope ts(K_DECODE_MERGE, st);
-    decode_merge_kernel<<<dim3(B, kHeads / kMergeHeads), kMergeThreads, 0, st>>>(
-        part, ml, seq_len, cache->seq_base, max_len > 0 ? cache->capacity : 0, B, max_len,
-        pairs, hi, lo);
-    s = launch_status();
-    if (s != MLA_OK) return s;
+    const uint64_t dims[2] = {(uint64_t)kDC, (uint64_t)kHeads * 128};
+    const uint64_t strides[1] = {(uint64_t)kDC * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!make_tmap(&tm_wuv, w->W_UV, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+      return MLA_ERR_CUDA;
   }
-
-  // 4. o = W^UV_i o~
-  return tc_unabsorb(d, w, hi, lo, B, o, K_UNABSORB, st);
+  s = unabsorb_setup();
+  if (s != MLA_OK) return s;
+  TraceScope ts(K_UNABSORB, st);
+  decode_unabsorb_kernel<<<dim3(kHeads, ceil_div(B, kUnBN)), kUnThreads, kUnSmem, st>>>(
+      tm_wuv, part, ml, rng, B + kMaxPairs, seq_len, cache->seq_base,
+      max_len > 0 ? cache->capacity : 0, B, max_len, o);
+  return launch_status();
 }
 
 }  // namespace mla

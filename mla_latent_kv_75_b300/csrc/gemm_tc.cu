@@ -143,9 +143,9 @@ __global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow
       }
       ++issued;
     }
-    // drain: every issued copy must land before the CTA may exit
+    // drain: every issued copy must land before the CTA may exit (even after an abort)
     for (int g = (issued > kStages ? issued - kStages : 0); g < issued; ++g)
-      mbar_wait(&full[g % kStages], (g / kStages) & 1, abort);
+      mbar_wait_drain(&full[g % kStages], (g / kStages) & 1);
   } else if (warp == 1) {
     // ---------------- MMA issuer (one elected lane of the converged warp)
     constexpr uint32_t idesc = idesc_f16(128, kAccN, 1, kMode == kGroupedMN ? 1 : 0, 0);
@@ -258,6 +258,8 @@ __global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow
   if (epi) tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    // the MMAs committed to `done` have completed before tensor memory is freed
+    mbar_wait_drain(done, 0);
     tc_fence_after();
     tmem_dealloc(tmem, tmem_cols);
   }
@@ -283,7 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* acc_full = empty + kStages;
   uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   constexpr int kAccN = kDual ? 2 * BN : BN;  // hi/lo: one MMA of width 2*BN (see above)
   constexpr uint32_t kCols = 2 * kAccN < 32 ? 32 : 2 * kAccN;
@@ -302,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 4);
     }
+    mbar_init(mma_done, 1);
     *abort = 0;
     fence_barrier_init();
   }
@@ -339,8 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued;
       }
     }
+    // drain: every issued copy must land before the CTA may exit (even after an abort)
     for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
-      mbar_wait(&full[k % kStages], (k / kStages) & 1, abort);
+      mbar_wait_drain(&full[k % kStages], (k / kStages) & 1);
   } else if (warp == 1) {
     // ---------------- MMA issuer (one elected lane of the converged warp)
     constexpr uint32_t idesc = idesc_f16(128, kAccN, 1, 0, 0);
@@ -377,6 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     }
+    // every MMA issued by this CTA completes before its tensor memory is freed
+    if (elect_one()) mma_commit(mma_done);
+    __syncwarp();
+    mbar_wait_drain(mma_done, 0);
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> registers -> global, overlapped with the next tile
     const int q = warp & 3;
@@ -460,11 +469,6 @@ struct EpStoreBF16 {
   }
 };
 
-struct EpStoreF32 {
-  float* y;
-  int64_t ld;
-  __device__ void operator()(int o, int n, float v, float) const { y[(int64_t)n * ld + o] = v; }
-};
 
 
 // Query up-projection: rows [0, n_h*d_hc) of [W^UQ; W^QR] are q^C, the rest q^R with RoPE.
@@ -782,14 +786,6 @@ mla_status_t tc_absorb(const mla_dims_t* d, const mla_weights_t* w, const void* 
   GroupArgs a{w->W_UK, d->n_h, d->d_c, d->d_hc, q_c, nullptr, B, kid};
   EpStoreBF16 ep{(__nv_bfloat16*)qt, nullptr, (int64_t)d->n_h * d->d_c};
   return launch_grouped<kGroupedMN>(a, ep, st);
-}
-
-// o[b, i, :] = W^UV_i o~[b, i, :] with o~ = hi + lo (two bf16 operands, one fp32 accumulator).
-mla_status_t tc_unabsorb(const mla_dims_t* d, const mla_weights_t* w, const void* ol_hi,
-                         const void* ol_lo, int B, float* o, int kid, cudaStream_t st) {
-  GroupArgs a{w->W_UV, d->n_h, d->d_hc, d->d_c, ol_hi, ol_lo, B, kid};
-  EpStoreF32 ep{o, (int64_t)d->n_h * d->d_hc};
-  return launch_grouped<kGroupedK>(a, ep, st);
 }
 
 }  // namespace mla

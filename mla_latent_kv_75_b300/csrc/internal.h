@@ -58,8 +58,6 @@ mla_status_t tc_q_up(const mla_dims_t* d, const mla_weights_t* w, const void* cq
                      bool f16_out, int kid, cudaStream_t st);
 mla_status_t tc_absorb(const mla_dims_t* d, const mla_weights_t* w, const void* q_c, int B,
                        void* qt, int kid, cudaStream_t st);
-mla_status_t tc_unabsorb(const mla_dims_t* d, const mla_weights_t* w, const void* ol_hi,
-                         const void* ol_lo, int B, float* o, int kid, cudaStream_t st);
 
 // Tensor-core causal prefill (V2 widths, bf16): prefill_tc.cu
 size_t tc_prefill_ws(const mla_dims_t* d, int n_tok);

@@ -18,6 +18,8 @@
 // 64 columns of the score buffer it came from); warps 2..5 run the online softmax, one thread
 // query row and column half (two warps per TMEM lane quarter, 64 key columns each), in log2
 // units with lazy rescaling of O.
+#include <mutex>
+
 #include "internal.h"
 #include "tc.cuh"
 
@@ -46,6 +48,7 @@ constexpr float kTau = 8.f;      // lazy rescale threshold (log2 units)
 
 struct Bars {
   uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done;
+  uint64_t mma_done;
   uint32_t tmem_slot;
   int abort;
   float row_max[2][2][kBQ];  // [tile parity][column half][row]: partial maxima of the halves
@@ -88,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.p_full[s], 8);
     }
     mbar_init(&sh.pv_done, 1);
+    mbar_init(&sh.mma_done, 1);
     sh.abort = 0;
     fence_barrier_init();
   }
@@ -126,12 +130,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(vb + kBox, &tm_v, &sh.v_full[s], 64, h, y);
       ++v_issued;
     }
-    // drain: every issued copy must land before the CTA may exit
-    mbar_wait(&sh.q_full, 0, abort);
+    // drain: every issued copy must land before the CTA may exit (even after an abort)
+    mbar_wait_drain(&sh.q_full, 0);
     for (int kt = (k_issued > 2 ? k_issued - 2 : 0); kt < k_issued; ++kt)
-      mbar_wait(&sh.k_full[kt & 1], (kt >> 1) & 1, abort);
+      mbar_wait_drain(&sh.k_full[kt & 1], (kt >> 1) & 1);
     for (int kt = (v_issued > 2 ? v_issued - 2 : 0); kt < v_issued; ++kt)
-      mbar_wait(&sh.v_full[kt & 1], (kt >> 1) & 1, abort);
+      mbar_wait_drain(&sh.v_full[kt & 1], (kt >> 1) & 1);
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc_s = idesc_f16(128, kBK, 1, 0, 0);  // A, B K-major
@@ -180,6 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the next score tile for this buffer is queued behind PV(kt), which reads P from it
       if (kt + 2 < n_kt && !issue_s(kt + 2)) break;
     }
+    // every MMA issued by this CTA completes before its tensor memory is freed
+    if (elect_one()) mma_commit(&sh.mma_done);
+    __syncwarp();
+    mbar_wait_drain(&sh.mma_done, 0);
   } else if (warp >= 2) {
     // ------------------------------------------------------------- softmax warps
     const int q = warp & 3;
@@ -375,14 +383,18 @@ mla_status_t tc_prefill(const mla_dims_t* d, const mla_weights_t* w, const void*
     if (!make_tmap(&tkr, lat, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
       return MLA_ERR_CUDA;
   }
-  static bool attr_done[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
-  if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(prefill_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return MLA_ERR_CUDA;
-    attr_done[dev] = true;
+  {
+    static std::mutex mu;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_done[dev]) {
+      if (cudaFuncSetAttribute(prefill_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes) != cudaSuccess)
+        return MLA_ERR_CUDA;
+      attr_done[dev] = true;
+    }
   }
   const float scale_log2 = softmax_scale(d) * 1.4426950408889634f;
   dim3 grid(ceil_div(max_T, kBQ), kH, B);
