@@ -1,7 +1,8 @@
 #!/usr/bin/env python3
 """Benchmark of the MLA hot path on B300: one decode step of the V2-shaped batch-16,
 context-4096 workload (append the 16 new tokens' latent rows, project their queries,
-weight-absorbed decode over the latent cache), plus the causal-prefill workload.
+weight-absorbed decode over the latent cache), the same step on the long-context and ragged
+decode workloads (one block each under "configs"), plus the causal-prefill workload.
 
 Prints ONE JSON line. ``--impl reference`` times the float64 CPU oracle instead (the
 baseline arm). Under torchrun every rank runs its own replica of the workload (decode
@@ -27,6 +28,7 @@ import mla_inputs as mi  # noqa: E402
 
 ROW_BYTES_BF16 = (512 + 64) * 2
 DEFAULT_WORKLOAD = "v2_decode_b16_l4096"
+EXTRA_DECODE_WORKLOADS = ("v2_decode_b1_l131072", "v2_decode_b4_l32768", "v2_decode_b128_ragged")
 PREFILL_WORKLOAD = "v2_prefill_b2_t4096"
 L2_FLUSH_BYTES = 256 << 20
 
@@ -51,14 +53,38 @@ def decode_kernel_costs(wl: mi.Workload):
                        flops=2 * B * d.n_h * d.d_hc * d.d_c),
         "decode_attn": dict(bytes=rows * d.row * e + B * d.n_h * (d.d_c + d.d_hr) * e,
                             flops=rows * (2 * d.n_h * d.row + 2 * d.n_h * d.d_c)),
-        # SIMT path: merge + W^UV in one kernel; tensor-core path: merge, then unabsorb
+        # merge of the split partials + W^UV: one SIMT kernel (decode_combine) or one
+        # tensor-core kernel (unabsorb); only the one that ran is counted
         "decode_combine": dict(bytes=nc * d.d_c * e + B * d.n_h * d.d_hc * 4,
                                flops=2 * B * d.n_h * d.d_hc * d.d_c),
-        "decode_merge": dict(bytes=0, flops=0),
         "unabsorb": dict(bytes=nc * d.d_c * e + B * d.n_h * d.d_hc * 4,
                          flops=2 * B * d.n_h * d.d_hc * d.d_c),
     }
     return out
+
+
+DECODE_CALL_KERNELS = ("absorb", "decode_attn", "decode_combine", "unabsorb")
+
+
+def build_info():
+    """Source identity of this run: the commit recorded by the library build (the GPU machine gets
+    a snapshot without .git), else the current commit, plus a hash of the CUDA sources."""
+    import hashlib
+    info = {}
+    try:
+        info = json.load(open(os.path.join(ROOT, "_build", "build_info.json")))
+    except Exception:
+        try:
+            info["git"] = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True,
+                                         text=True, timeout=10).stdout.strip() or None
+        except Exception:
+            info["git"] = None
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "mla_latent_kv_75_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    info["sources_sha1"] = h.hexdigest()
+    return info
 
 
 def prefill_flops(wl: mi.Workload):
@@ -222,7 +248,7 @@ def run_reference(args, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * statistics.mean(times), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(wl, reference=True),
+        "config": workload_config(wl), "timing": ORACLE_TIMING,
         "cpu_baseline": {"value": sig(value), "unit": "GB/s", "cores": blas_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": sig(value), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -253,16 +279,16 @@ def metric_name():
     return "MLA decode cache GB/s + TFLOP/s (% roofline) on 1 B300; prefill TFLOP/s"
 
 
-def workload_config(wl, reference=False):
-    cfg = {"workload": wl.name, "B": wl.B, "context": int(max(wl.seq_lens)),
-           "cache_rows": wl.n_rows, "dims": "d=5120 n_h=128 d_hc=128 d_hr=64 d_c=512 d_cq=1536",
-           "step": "append B new rows + project B queries + absorbed decode"}
-    if reference:
-        cfg["launch"] = "float64 CPU oracle (explicit per-head form) on the host cores"
-    else:
-        cfg["launch"] = "CUDA graph of the library calls (e2e: eager calls + H2D/D2H copies)"
-        cfg["l2"] = "flushed between timed steps (256 MB write, then 256 MB read)"
-    return cfg
+def workload_config(wl):
+    """The workload; identical in both arms (how each arm runs it is under "timing")."""
+    return {"workload": wl.name, "B": wl.B, "context": int(max(wl.seq_lens)),
+            "cache_rows": wl.n_rows, "dims": "d=5120 n_h=128 d_hc=128 d_hr=64 d_c=512 d_cq=1536",
+            "step": "append B new rows + project B queries + absorbed decode"}
+
+
+GPU_TIMING = {"launch": "CUDA graph of the library calls (e2e: eager calls + H2D/D2H copies)",
+              "l2": "flushed between timed steps (256 MB write, then 256 MB read)"}
+ORACLE_TIMING = {"launch": "float64 CPU oracle (explicit per-head form) on the host cores"}
 
 
 def sig(x, n=4):
@@ -318,25 +344,58 @@ def time_steps(fn, steps, flush, trace_capacity=0, hold_ms=0.0):
     return ms, (trace.launches() if trace else [])
 
 
-def run_ours(args, rank, world, local_rank):
+def kernel_table(launches, costs, peaks):
+    """Per-kernel launches, mean device time, share of traced time and, for kernels with an
+    algorithmic cost, GB/s, TFLOP/s and the fraction of their own roofline."""
+    per = {}
+    for name, t in launches:
+        per.setdefault(name, []).append(t)
+    total = sum(sum(v) for v in per.values()) or 1.0
+    kernels = {}
+    for name, ts in per.items():
+        avg_ms = statistics.mean(ts)
+        entry = {"launches": len(ts), "avg_us": round(avg_ms * 1e3, 3),
+                 "share": round(sum(ts) / total, 4)}
+        c = costs.get(name)
+        if c and c["bytes"] > 0:
+            floor_s = max(c["bytes"] / (peaks["hbm_gbs"] * 1e9),
+                          c["flops"] / (peaks["bf16_tflops"] * 1e12))
+            entry.update({"alg_bytes": c["bytes"], "alg_flops": c["flops"],
+                          "GB_s": round(c["bytes"] / (avg_ms * 1e-3) / 1e9, 1),
+                          "TFLOP_s": round(c["flops"] / (avg_ms * 1e-3) / 1e12, 2),
+                          "roofline_frac": round(floor_s / (avg_ms * 1e-3), 4)})
+        kernels[name] = entry
+    return per, kernels
+
+
+def roofline_of(name, per, costs, peaks, workload):
+    """Roofline object of kernel ``name``: algorithmic bytes (or flops) per launch over its mean
+    CUDA-event duration, against the measured peak of the bound it sits under."""
+    c = costs[name]
+    avg_s = statistics.mean(per[name]) * 1e-3
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if c["flops"] / c["bytes"] < ridge:
+        achieved = c["bytes"] / avg_s / 1e9
+        r = {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1),
+             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = c["flops"] / avg_s / 1e12
+        r = {"kernel": name, "bound": "tensor", "achieved": round(achieved, 2),
+             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+             "frac": round(achieved / peaks["bf16_tflops"], 4)}
+    r["peak_source"] = peaks["source"]
+    r["traffic"] = measured_traffic(name, workload)
+    return r
+
+
+def measure_decode(wl, args, dev, peaks, flush, world, steps, want_cpu, cpu_seconds,
+                   cpu_heads=16, cpu_max_seqs=0):
+    """One decode workload: the graph-timed step, per-kernel device times, the e2e step and
+    (rank 0, one GPU) the oracle on a bounded sample. Frees its device buffers on return."""
     import torch
-    import torch.distributed as dist
     import mla_latent_kv_75_b300 as mla
-    from mla_latent_kv_75_b300 import host
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    wl = mi.workload(args.workload)
-    peaks = load_peaks()
     step, h_dev, h_host, o_host = setup_decode(wl, dev)
-    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    clean_buf = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def flush():
-        # Write a buffer larger than L2, then read another: no step data stays in L2, and no
-        # dirty flush lines are left for the timed step to write back.
-        flush_buf.zero_()
-        clean_buf.sum()
 
     def one_step():
         step.step(h_dev)
@@ -363,115 +422,116 @@ def run_ours(args, rank, world, local_rank):
             graph.replay()
         torch.cuda.synchronize()
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        if graph is not None:
-            ms, _ = time_steps(graph.replay, args.steps, flush)
-        else:
-            ms, _ = time_steps(one_step, args.steps, flush)
-        # Per-kernel device times: the same step as eager library calls, each enqueued behind a
-        # sleep kernel so that the host never starves the GPU between launches; CUDA event pairs
-        # around every launch (on its stream) then time the kernels alone.
-        _, launches = time_steps(one_step, args.steps, flush, trace_capacity=64 * args.steps,
-                                 hold_ms=0.5)
+    ms, _ = time_steps(graph.replay if graph is not None else one_step, steps, flush)
+    # Per-kernel device times: the same step as eager library calls, each enqueued behind a
+    # sleep kernel so that the host never starves the GPU between launches; CUDA event pairs
+    # around every launch (on its stream) then time the kernels alone.
+    _, launches = time_steps(one_step, steps, flush, trace_capacity=64 * steps, hold_ms=0.5)
     torch.cuda.synchronize()
     assert mla.mla_get_device_status() == 0
-    if world > 1:
-        dist.barrier()
     total_ms = max_over_ranks(sum(ms), world, dev)
-    clocks = clk.summary()
-    ms_step = total_ms / args.steps
 
     for _ in range(3):
         flush()
         one_e2e()
-    e2e_ms, _ = time_steps(one_e2e, args.steps, flush)
+    e2e_ms, _ = time_steps(one_e2e, steps, flush)
     e2e_total = max_over_ranks(sum(e2e_ms), world, dev)
 
     costs = decode_kernel_costs(wl)
     e = 2 if wl.dtype == "bf16" else 4
     cache_bytes = wl.n_rows * wl.dims.row * e
-    step_flops = sum(c["flops"] for c in costs.values())
-    value = job_rate(world, cache_bytes, args.steps, total_ms)
-    e2e_value = job_rate(world, cache_bytes, args.steps, e2e_total)
-
-    # per-kernel breakdown from the launch trace
-    per = {}
-    for name, t in launches:
-        per.setdefault(name, []).append(t)
-    kernels = {}
-    for name, ts in per.items():
-        avg_ms = statistics.mean(ts)
-        c = costs.get(name)
-        entry = {"launches": len(ts), "avg_us": round(avg_ms * 1e3, 3),
-                 "share": round(sum(ts) / sum(sum(v) for v in per.values()), 4)}
-        if c and c["bytes"] > 0:
-            gbs = c["bytes"] / (avg_ms * 1e-3) / 1e9
-            tfl = c["flops"] / (avg_ms * 1e-3) / 1e12
-            floor_s = max(c["bytes"] / (peaks["hbm_gbs"] * 1e9),
-                          c["flops"] / (peaks["bf16_tflops"] * 1e12))
-            entry.update({"alg_bytes": c["bytes"], "alg_flops": c["flops"],
-                          "GB_s": round(gbs, 1), "TFLOP_s": round(tfl, 2),
-                          "roofline_frac": round(floor_s / (avg_ms * 1e-3), 4)})
-        kernels[name] = entry
+    per, kernels = kernel_table(launches, costs, peaks)
+    step_flops = sum(costs[n]["flops"] for n in per if n in costs)
     dominant = max(per, key=lambda n: sum(per[n])) if per else None
-    roofline = None
-    if dominant and dominant in costs:
-        c = costs[dominant]
-        avg_s = statistics.mean(per[dominant]) * 1e-3
-        ai = c["flops"] / c["bytes"]
-        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-        if ai < ridge:
-            achieved = c["bytes"] / avg_s / 1e9
-            roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1),
-                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(achieved / peaks["hbm_gbs"], 4)}
-        else:
-            achieved = c["flops"] / avg_s / 1e12
-            roofline = {"kernel": dominant, "bound": "tensor", "achieved": round(achieved, 2),
-                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                        "frac": round(achieved / peaks["bf16_tflops"], 4)}
-        roofline["peak_source"] = peaks["source"]
-        roofline["traffic"] = measured_traffic(dominant, wl.name)
+    roofline = roofline_of(dominant, per, costs, peaks, wl.name) if dominant in costs else None
 
-    # the absorbed-decode call alone (absorb + attention + combine)
-    dec_names = ("absorb", "decode_attn", "decode_combine", "decode_merge", "unabsorb")
-    dec_s = sum(statistics.mean(per[n]) for n in dec_names if n in per) * 1e-3
-    dec_bytes = sum(costs[n]["bytes"] for n in dec_names if n in per)
-    dec_flops = sum(costs[n]["flops"] for n in dec_names if n in per)
+    # the absorbed-decode call alone (absorb + attention + merge/un-absorb)
+    dec = [n for n in DECODE_CALL_KERNELS if n in per]
+    dec_s = sum(statistics.mean(per[n]) for n in dec) * 1e-3
+    dec_bytes = sum(costs[n]["bytes"] for n in dec)
+    dec_flops = sum(costs[n]["flops"] for n in dec)
     decode_call = None
     if dec_s > 0:
-        floor_s = max(dec_bytes / (peaks["hbm_gbs"] * 1e9), dec_flops / (peaks["bf16_tflops"] * 1e12))
-        decode_call = {"us": round(dec_s * 1e6, 2), "cache_GB_s": round(cache_bytes / dec_s / 1e9, 1),
+        floor_s = max(dec_bytes / (peaks["hbm_gbs"] * 1e9),
+                      dec_flops / (peaks["bf16_tflops"] * 1e12))
+        decode_call = {"kernels": dec, "us": round(dec_s * 1e6, 2), "floor_us": round(floor_s * 1e6, 2),
+                       "alg_bytes": dec_bytes, "alg_flops": dec_flops,
+                       "cache_GB_s": round(cache_bytes / dec_s / 1e9, 1),
                        "TFLOP_s": round(dec_flops / dec_s / 1e12, 2),
                        "roofline_frac": round(floor_s / dec_s, 4)}
+    step_bytes = sum(costs[n]["bytes"] for n in per if n in costs)
+    out = {
+        "value": round(job_rate(world, cache_bytes, steps, total_ms), 2), "unit": "GB/s",
+        "ms_per_step": round(total_ms / steps, 4), "steps": steps,
+        "tflops": round(world * step_flops * steps / (total_ms * 1e-3) / 1e12, 3),
+        "step_alg_bytes": step_bytes,
+        "step_roofline_frac": round(step_bytes / (peaks["hbm_gbs"] * 1e9) / (total_ms / steps * 1e-3), 4),
+        "config": workload_config(wl), "roofline": roofline, "decode_call": decode_call,
+        "kernels": kernels, "gpu_launches": len(launches),
+        "e2e": {"value": round(job_rate(world, cache_bytes, steps, e2e_total), 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h_host.numel() * h_host.element_size()),
+                "d2h_bytes_per_step": int(o_host.numel() * o_host.element_size()),
+                "ms_per_step": round(e2e_total / steps, 4)},
+        "fast_path": mla.mla_fast_path(step.model.abi_dims),
+    }
+    del graph, step, h_dev, h_host, o_host
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if want_cpu:
+        v, spent, sample = oracle_decode_sample(wl, cpu_seconds, n_heads=cpu_heads,
+                                               max_seqs=cpu_max_seqs)
+        out["cpu_baseline"] = {"value": sig(v), "unit": "GB/s", "cores": blas_threads(),
+                               "kind": "oracle", "sample": sample, "seconds": round(spent, 2)}
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import mla_latent_kv_75_b300 as mla  # noqa: F401  (fails loudly without the library)
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean_buf = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        # Write a buffer larger than L2, then read another: no step data stays in L2, and no
+        # dirty flush lines are left for the timed step to write back.
+        flush_buf.zero_()
+        clean_buf.sum()
+
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        main = measure_decode(mi.workload(args.workload), args, dev, peaks, flush, world,
+                              args.steps, want_cpu, args.cpu_seconds)
+        configs = {}
+        if not args.no_extra_configs and args.workload == DEFAULT_WORKLOAD:
+            for name in EXTRA_DECODE_WORKLOADS:
+                configs[name] = measure_decode(mi.workload(name), args, dev, peaks, flush, world,
+                                               max(1, min(args.steps, args.extra_steps)), want_cpu,
+                                               args.extra_cpu_seconds, cpu_heads=4, cpu_max_seqs=1)
+    clocks = clk.summary()
 
     prefill = None
     if not args.no_prefill:
         prefill = run_prefill(args, dev, peaks, flush)
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, spent, sample = oracle_decode_sample(wl, args.cpu_seconds)
-        cpu = {"value": sig(v), "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": sample, "seconds": round(spent, 2)}
-
     if rank == 0:
         line = {
-            "metric": metric_name(), "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "metric": metric_name(), "value": main["value"], "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": workload_config(wl),
-            "tflops": round(world * step_flops * args.steps / (total_ms * 1e-3) / 1e12, 3),
-            "roofline": roofline, "decode_call": decode_call, "kernels": kernels,
-            "prefill": prefill, "cpu_baseline": cpu,
-            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
-                    "h2d_bytes_per_step": int(h_host.numel() * h_host.element_size()),
-                    "d2h_bytes_per_step": int(o_host.numel() * o_host.element_size()),
-                    "ms_per_step": round(e2e_total / args.steps, 4)},
-            "gpu_launches": len(launches), "clocks": clocks,
-            "fast_path": mla.mla_fast_path(step.model.abi_dims),
+            "data": "synthetic", "config": main["config"], "timing": GPU_TIMING,
+            "tflops": main["tflops"], "roofline": main["roofline"],
+            "decode_call": main["decode_call"], "step_roofline_frac": main["step_roofline_frac"],
+            "kernels": main["kernels"], "configs": configs, "prefill": prefill,
+            "cpu_baseline": main.get("cpu_baseline"), "e2e": main["e2e"],
+            "gpu_launches": main["gpu_launches"], "clocks": clocks, "fast_path": main["fast_path"],
+            "build": build_info(),
         }
         print(json.dumps(line), flush=True)
 
@@ -521,6 +581,11 @@ def main():
     ap.add_argument("--no-graph", action="store_true",
                     help="time the decode step as eager library calls instead of a CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="skip the long-context and ragged decode workloads")
+    ap.add_argument("--extra-steps", type=int, default=10,
+                    help="timed steps of each extra decode workload")
+    ap.add_argument("--extra-cpu-seconds", type=float, default=4.0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

@@ -65,7 +65,26 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
     os.replace(tmp, LIB)
+    _write_build_info()
     return LIB
+
+
+def _write_build_info() -> None:
+    """Record the commit the library was built from (the GPU machine receives the tree without
+    its .git directory); reporting only."""
+    import json
+    info = {"git": None, "dirty": None}
+    try:
+        sha = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True,
+                             text=True, timeout=10)
+        st = subprocess.run(["git", "-C", ROOT, "status", "--porcelain", "--", "mla_latent_kv_75_b300",
+                             "include"], capture_output=True, text=True, timeout=10)
+        if sha.returncode == 0:
+            info = {"git": sha.stdout.strip(), "dirty": bool(st.stdout.strip())}
+    except Exception:
+        pass
+    with open(os.path.join(BUILD, "build_info.json"), "w") as f:
+        json.dump(info, f)
 
 
 if __name__ == "__main__":
