@@ -51,6 +51,13 @@ def decode_kernel_costs(wl: mi.Workload):
                      flops=2 * B * d.d_cq * (nc + nr)),
         "absorb": dict(bytes=nc * d.d_c * e + B * nc * e + B * d.n_h * d.d_c * e,
                        flops=2 * B * d.n_h * d.d_hc * d.d_c),
+        # fused step: append + c^Q in one launch (W^DKV, W^KR, W^DQ read once) ...
+        "down": dict(bytes=((d.row + d.d_cq) * d.d + B * d.d + B * d.row) * e + B * d.d_cq * 4,
+                     flops=2 * B * d.d * (d.row + d.d_cq)),
+        # ... and the query up-projection with the absorption applied (q^C stays on chip)
+        "q_absorb": dict(bytes=((nc + nr) * d.d_cq + nc * d.d_c) * e
+                         + B * d.d_cq * 4 + B * (d.n_h * d.d_c + nr) * e,
+                         flops=2 * B * d.d_cq * (nc + nr) + 2 * B * d.n_h * d.d_hc * d.d_c),
         "decode_attn": dict(bytes=rows * d.row * e + B * d.n_h * (d.d_c + d.d_hr) * e,
                             flops=rows * (2 * d.n_h * d.row + 2 * d.n_h * d.d_c)),
         # merge of the split partials + W^UV: one SIMT kernel (decode_combine) or one
@@ -283,7 +290,8 @@ def workload_config(wl):
     """The workload; identical in both arms (how each arm runs it is under "timing")."""
     return {"workload": wl.name, "B": wl.B, "context": int(max(wl.seq_lens)),
             "cache_rows": wl.n_rows, "dims": "d=5120 n_h=128 d_hc=128 d_hr=64 d_c=512 d_cq=1536",
-            "step": "append B new rows + project B queries + absorbed decode"}
+            "step": "append B new rows + project B queries (absorbed) + decode over the latent "
+                    "cache (mla_decode_step)"}
 
 
 GPU_TIMING = {"launch": "CUDA graph of the library calls (e2e: eager calls + H2D/D2H copies)",
@@ -297,6 +305,8 @@ def sig(x, n=4):
 
 
 def setup_decode(wl, dev):
+    """Device weights, the latent cache filled by mla_append_cache over every context token,
+    and two steps over it: the one-call fused step and the three-call step."""
     import torch
     from mla_latent_kv_75_b300 import host
     d = wl.dims
@@ -306,14 +316,15 @@ def setup_decode(wl, dev):
     cache = host.LatentCache(d, wl.dtype, base, wl.n_rows, device=dev)
     host.fill_context(model, cache, lambda b, n: mi.hidden(d, wl.dtype, b, n, wl.seed),
                       wl.seq_lens)
-    step = host.DecodeStep(model, cache, wl.seq_lens)
+    step = host.DecodeStep(model, cache, wl.seq_lens, fused=True)
+    step3 = host.DecodeStep(model, cache, wl.seq_lens)
     h_new = np.stack([mi.hidden_rows(d, wl.dtype, b, [L - 1], wl.seed)[0]
                       for b, L in enumerate(wl.seq_lens)])
     h_dev = host.to_device(h_new, wl.dtype, dev)
     h_host = host.to_device(h_new, wl.dtype, "cpu", pin=True)
     o_host = torch.empty(step.o.shape, dtype=step.o.dtype).pin_memory()
     torch.cuda.synchronize()
-    return step, h_dev, h_host, o_host
+    return step, step3, h_dev, h_host, o_host
 
 
 def time_steps(fn, steps, flush, trace_capacity=0, hold_ms=0.0):
@@ -388,96 +399,111 @@ def roofline_of(name, per, costs, peaks, workload):
     return r
 
 
+def call_block(names, per, costs, peaks, cache_bytes):
+    """Time, floor and roofline fraction of a group of kernels (one library call)."""
+    dec = [n for n in names if n in per]
+    dec_s = sum(statistics.mean(per[n]) for n in dec) * 1e-3
+    if dec_s <= 0:
+        return None
+    dec_bytes = sum(costs[n]["bytes"] for n in dec)
+    dec_flops = sum(costs[n]["flops"] for n in dec)
+    floor_s = max(dec_bytes / (peaks["hbm_gbs"] * 1e9), dec_flops / (peaks["bf16_tflops"] * 1e12))
+    return {"kernels": dec, "us": round(dec_s * 1e6, 2), "floor_us": round(floor_s * 1e6, 2),
+            "alg_bytes": dec_bytes, "alg_flops": dec_flops,
+            "cache_GB_s": round(cache_bytes / dec_s / 1e9, 1),
+            "TFLOP_s": round(dec_flops / dec_s / 1e12, 2), "roofline_frac": round(floor_s / dec_s, 4)}
+
+
 def measure_decode(wl, args, dev, peaks, flush, world, steps, want_cpu, cpu_seconds,
                    cpu_heads=16, cpu_max_seqs=0):
-    """One decode workload: the graph-timed step, per-kernel device times, the e2e step and
-    (rank 0, one GPU) the oracle on a bounded sample. Frees its device buffers on return."""
+    """One decode workload: the graph-timed step (the one-call fused step, mla_decode_step; the
+    three-call step beside it), per-kernel device times of both, the e2e step and (rank 0, one
+    GPU) the oracle on a bounded sample. Frees its device buffers on return."""
     import torch
     import mla_latent_kv_75_b300 as mla
 
-    step, h_dev, h_host, o_host = setup_decode(wl, dev)
+    step, step3, h_dev, h_host, o_host = setup_decode(wl, dev)
 
-    def one_step():
-        step.step(h_dev)
-
-    def one_e2e():
+    def e2e_step():
         h_dev.copy_(h_host, non_blocking=True)
         step.step(h_dev)
         o_host.copy_(step.o, non_blocking=True)
 
-    for _ in range(max(3, args.warmup)):
-        flush()
-        one_step()
-    assert mla.mla_get_device_status() == 0
+    def graph_of(st):
+        for _ in range(max(3, args.warmup)):
+            flush()
+            st.step(h_dev)
+        assert mla.mla_get_device_status() == 0
+        if args.no_graph:
+            return lambda: st.step(h_dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            st.step(h_dev)
+        for _ in range(max(3, args.warmup)):
+            flush()
+            g.replay()
+        torch.cuda.synchronize()
+        return g.replay
 
     # The timed decode step is a CUDA graph of the library's launches (how a decode loop runs in
     # production: no host work between kernels).
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            one_step()
-        for _ in range(max(3, args.warmup)):
-            flush()
-            graph.replay()
-        torch.cuda.synchronize()
+    run_f, run_3 = graph_of(step), graph_of(step3)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    ms, _ = time_steps(graph.replay if graph is not None else one_step, steps, flush)
-    # Per-kernel device times: the same step as eager library calls, each enqueued behind a
+    ms, _ = time_steps(run_f, steps, flush)
+    ms3, _ = time_steps(run_3, steps, flush)
+    # Per-kernel device times: the same steps as eager library calls, each enqueued behind a
     # sleep kernel so that the host never starves the GPU between launches; CUDA event pairs
     # around every launch (on its stream) then time the kernels alone.
-    _, launches = time_steps(one_step, steps, flush, trace_capacity=64 * steps, hold_ms=0.5)
+    _, launches = time_steps(lambda: step.step(h_dev), steps, flush, trace_capacity=64 * steps,
+                             hold_ms=0.5)
+    _, launches3 = time_steps(lambda: step3.step(h_dev), steps, flush,
+                              trace_capacity=64 * steps, hold_ms=0.5)
     torch.cuda.synchronize()
     assert mla.mla_get_device_status() == 0
     total_ms = max_over_ranks(sum(ms), world, dev)
+    total3_ms = max_over_ranks(sum(ms3), world, dev)
 
     for _ in range(3):
         flush()
-        one_e2e()
-    e2e_ms, _ = time_steps(one_e2e, steps, flush)
+        e2e_step()
+    e2e_ms, _ = time_steps(e2e_step, steps, flush)
     e2e_total = max_over_ranks(sum(e2e_ms), world, dev)
 
     costs = decode_kernel_costs(wl)
     e = 2 if wl.dtype == "bf16" else 4
     cache_bytes = wl.n_rows * wl.dims.row * e
     per, kernels = kernel_table(launches, costs, peaks)
+    per3, kernels3 = kernel_table(launches3, costs, peaks)
     step_flops = sum(costs[n]["flops"] for n in per if n in costs)
+    step_bytes = sum(costs[n]["bytes"] for n in per if n in costs)
     dominant = max(per, key=lambda n: sum(per[n])) if per else None
     roofline = roofline_of(dominant, per, costs, peaks, wl.name) if dominant in costs else None
-
-    # the absorbed-decode call alone (absorb + attention + merge/un-absorb)
-    dec = [n for n in DECODE_CALL_KERNELS if n in per]
-    dec_s = sum(statistics.mean(per[n]) for n in dec) * 1e-3
-    dec_bytes = sum(costs[n]["bytes"] for n in dec)
-    dec_flops = sum(costs[n]["flops"] for n in dec)
-    decode_call = None
-    if dec_s > 0:
-        floor_s = max(dec_bytes / (peaks["hbm_gbs"] * 1e9),
-                      dec_flops / (peaks["bf16_tflops"] * 1e12))
-        decode_call = {"kernels": dec, "us": round(dec_s * 1e6, 2), "floor_us": round(floor_s * 1e6, 2),
-                       "alg_bytes": dec_bytes, "alg_flops": dec_flops,
-                       "cache_GB_s": round(cache_bytes / dec_s / 1e9, 1),
-                       "TFLOP_s": round(dec_flops / dec_s / 1e12, 2),
-                       "roofline_frac": round(floor_s / dec_s, 4)}
-    step_bytes = sum(costs[n]["bytes"] for n in per if n in costs)
     out = {
         "value": round(job_rate(world, cache_bytes, steps, total_ms), 2), "unit": "GB/s",
         "ms_per_step": round(total_ms / steps, 4), "steps": steps,
         "tflops": round(world * step_flops * steps / (total_ms * 1e-3) / 1e12, 3),
         "step_alg_bytes": step_bytes,
         "step_roofline_frac": round(step_bytes / (peaks["hbm_gbs"] * 1e9) / (total_ms / steps * 1e-3), 4),
-        "config": workload_config(wl), "roofline": roofline, "decode_call": decode_call,
+        "config": workload_config(wl), "roofline": roofline,
+        # the mla_decode_absorbed call (absorb + attention + merge/un-absorb), from the
+        # three-call step; and the latent decode of the fused step (attention + merge/un-absorb)
+        "decode_call": call_block(DECODE_CALL_KERNELS, per3, costs, peaks, cache_bytes),
+        "decode_latent_call": call_block(("decode_attn", "decode_combine", "unabsorb"), per, costs,
+                                         peaks, cache_bytes),
         "kernels": kernels, "gpu_launches": len(launches),
+        "three_call_step": {"ms_per_step": round(total3_ms / steps, 4),
+                            "value": round(job_rate(world, cache_bytes, steps, total3_ms), 2),
+                            "kernels": kernels3},
         "e2e": {"value": round(job_rate(world, cache_bytes, steps, e2e_total), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h_host.numel() * h_host.element_size()),
                 "d2h_bytes_per_step": int(o_host.numel() * o_host.element_size()),
-                "ms_per_step": round(e2e_total / steps, 4)},
+                "ms_per_step": round(e2e_total / steps, 4), "call": "mla_decode_step"},
         "fast_path": mla.mla_fast_path(step.model.abi_dims),
     }
-    del graph, step, h_dev, h_host, o_host
+    del run_f, run_3, step, step3, h_dev, h_host, o_host
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     if want_cpu:
@@ -527,8 +553,9 @@ def run_ours(args, rank, world, local_rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": main["config"], "timing": GPU_TIMING,
             "tflops": main["tflops"], "roofline": main["roofline"],
-            "decode_call": main["decode_call"], "step_roofline_frac": main["step_roofline_frac"],
-            "kernels": main["kernels"], "configs": configs, "prefill": prefill,
+            "decode_call": main["decode_call"], "decode_latent_call": main["decode_latent_call"],
+            "step_roofline_frac": main["step_roofline_frac"], "kernels": main["kernels"],
+            "three_call_step": main["three_call_step"], "configs": configs, "prefill": prefill,
             "cpu_baseline": main.get("cpu_baseline"), "e2e": main["e2e"],
             "gpu_launches": main["gpu_launches"], "clocks": clocks, "fast_path": main["fast_path"],
             "build": build_info(),

@@ -134,6 +134,48 @@ mla_status_t mla_decode_absorbed(const mla_dims_t* dims, const mla_weights_t* w,
                                  const int32_t* seq_len, int32_t B, int32_t max_len,
                                  void* ws, size_t ws_bytes, float* o, void* stream);
 
+/* Query projection with the absorption applied ([notes] §三分支计算 ① Query; [llama] §六: W^UQ and
+ * W^UK are fixed, so W^UK can be moved onto the query by associativity):
+ *   c^Q = W^DQ h,  q~_{t,i} = (W^UK_i)^T (W^UQ_i c^Q)   (d_c wide),  q^R_{t,i} = RoPE(W^QR_i c^Q),
+ * without writing q^C to global memory. h [n, d]; pos [n] device int32; outputs q_t
+ * [n, n_h, d_c] and q_r [n, n_h, d_h^R] in dtype. Workspace: mla_project_q_workspace_size(n)
+ * (c^Q kept above bf16 precision). Uses W_DQ, W_UQ, W_QR, W_UK. Tensor-core path only (V2
+ * widths in bf16, mla_fast_path(dims) == 1); other dims return MLA_ERR_UNSUPPORTED. */
+mla_status_t mla_project_q_absorbed(const mla_dims_t* dims, const mla_weights_t* w,
+                                    const void* h, const int32_t* pos, int32_t n, void* ws,
+                                    size_t ws_bytes, void* q_t, void* q_r, void* stream);
+
+/* mla_decode_absorbed for a caller that already holds the absorbed query q~ (for example from
+ * mla_project_q_absorbed): q_t [B, n_h, d_c] and q_r [B, n_h, d_h^R] in dtype; the scores,
+ * softmax, latent sum and o = W^UV_i o~ are those of mla_decode_absorbed. Workspace:
+ * mla_decode_workspace_size(B, max_len). Uses W_UV only. Tensor-core path only; other dims
+ * return MLA_ERR_UNSUPPORTED. */
+mla_status_t mla_decode_absorbed_latent(const mla_dims_t* dims, const mla_weights_t* w,
+                                        const void* q_t, const void* q_r,
+                                        const mla_cache_t* cache, const int32_t* seq_len,
+                                        int32_t B, int32_t max_len, void* ws, size_t ws_bytes,
+                                        float* o, void* stream);
+
+/* Workspace needed by mla_decode_step for B sequences of at most max_len rows. */
+mla_status_t mla_decode_step_workspace_size(const mla_dims_t* dims, int32_t B, int32_t max_len,
+                                            size_t* bytes);
+
+/* One decode step for B sequences, each with one new token ([notes] §三分支计算 ①–④ with the
+ * absorbed decode of [llama] §六): token b of h [B, d] is sequence b's token at position pos[b]
+ * (device int32 [B]).
+ *   1. the cache row seq_base[b] + pos[b] <- [W^DKV h_b ; RoPE(W^KR h_b)] and c^Q = W^DQ h_b,
+ *      in one launch (the three down-projections share their input);
+ *   2. q~ and q^R as in mla_project_q_absorbed;
+ *   3. the decode of mla_decode_absorbed_latent over seq_len[b] rows (normally pos[b] + 1, so
+ *      the new token's own row is the last one attended).
+ * Output o [B, n_h, d_h^C] float32. Workspace: mla_decode_step_workspace_size(B, max_len).
+ * Uses all seven matrices. Tensor-core path only; other dims return MLA_ERR_UNSUPPORTED (use
+ * mla_append_cache, mla_project_q and mla_decode_absorbed). */
+mla_status_t mla_decode_step(const mla_dims_t* dims, const mla_weights_t* w, const void* h,
+                             const int32_t* pos, mla_cache_t* cache, const int32_t* seq_len,
+                             int32_t B, int32_t max_len, void* ws, size_t ws_bytes, float* o,
+                             void* stream);
+
 /* Scratch capacity of mla_decode_absorbed_static, in bytes (32 MiB). */
 #define MLA_STATIC_WS_BYTES (32u << 20)
 

@@ -68,6 +68,11 @@ _SIGS = {
     "mla_prefill_workspace_size": [_PD, _I, _I, _I, _SZ],
     "mla_prefill": [_PD, _PW, _P, _P, _I, _I, _I, _PC, _P, ctypes.c_size_t, _P, _P],
     "mla_decode_absorbed_static": [_PD, _PW, _P, _P, _PC, _P, _I, _I, _P, _P],
+    "mla_project_q_absorbed": [_PD, _PW, _P, _P, _I, _P, ctypes.c_size_t, _P, _P, _P],
+    "mla_decode_absorbed_latent": [_PD, _PW, _P, _P, _PC, _P, _I, _I, _P, ctypes.c_size_t, _P,
+                                   _P],
+    "mla_decode_step_workspace_size": [_PD, _I, _I, _SZ],
+    "mla_decode_step": [_PD, _PW, _P, _P, _PC, _P, _I, _I, _P, ctypes.c_size_t, _P, _P],
     "mla_get_device_status": [_P],
     "mla_fast_path": [_PD],
 }
@@ -167,6 +172,35 @@ def mla_decode_absorbed(dims, weights, q_c, q_r, cache, seq_len, B, max_len, ws,
                                     _ptr(q_r), ctypes.byref(cache), _ptr(seq_len), int(B),
                                     int(max_len), _ptr(ws), int(ws_bytes), _ptr(o),
                                     _stream(stream)), "mla_decode_absorbed")
+
+
+def mla_project_q_absorbed(dims, weights, h, pos, n, ws, ws_bytes, q_t, q_r, stream=None) -> None:
+    _check(_lib.mla_project_q_absorbed(ctypes.byref(dims), ctypes.byref(weights), _ptr(h),
+                                       _ptr(pos), int(n), _ptr(ws), int(ws_bytes), _ptr(q_t),
+                                       _ptr(q_r), _stream(stream)), "mla_project_q_absorbed")
+
+
+def mla_decode_absorbed_latent(dims, weights, q_t, q_r, cache, seq_len, B, max_len, ws, ws_bytes,
+                               o, stream=None) -> None:
+    _check(_lib.mla_decode_absorbed_latent(ctypes.byref(dims), ctypes.byref(weights), _ptr(q_t),
+                                           _ptr(q_r), ctypes.byref(cache), _ptr(seq_len),
+                                           int(B), int(max_len), _ptr(ws), int(ws_bytes),
+                                           _ptr(o), _stream(stream)), "mla_decode_absorbed_latent")
+
+
+def mla_decode_step_workspace_size(dims, B, max_len) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.mla_decode_step_workspace_size(ctypes.byref(dims), int(B), int(max_len),
+                                               ctypes.byref(out)), "mla_decode_step_workspace_size")
+    return out.value
+
+
+def mla_decode_step(dims, weights, h, pos, cache, seq_len, B, max_len, ws, ws_bytes, o,
+                    stream=None) -> None:
+    _check(_lib.mla_decode_step(ctypes.byref(dims), ctypes.byref(weights), _ptr(h), _ptr(pos),
+                                ctypes.byref(cache), _ptr(seq_len), int(B), int(max_len),
+                                _ptr(ws), int(ws_bytes), _ptr(o), _stream(stream)),
+           "mla_decode_step")
 
 
 MLA_STATIC_WS_BYTES = 32 << 20

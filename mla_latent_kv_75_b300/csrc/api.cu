@@ -63,7 +63,7 @@ TraceState g_trace;
 const char* const kKernelNames[K_NUM_IDS] = {
     "append", "q_down", "q_up", "absorb", "decode_attn", "decode_combine", "token_map",
     "prefill_append", "prefill_q_down", "prefill_q_up", "expand_k", "expand_v", "prefill_attn",
-    "decode_merge", "unabsorb"};
+    "decode_merge", "unabsorb", "q_absorb", "down"};
 }  // namespace
 
 void trace_before(int kernel_id, cudaStream_t st) {
@@ -186,6 +186,103 @@ mla_status_t mla_decode_absorbed(const mla_dims_t* d, const mla_weights_t* w, co
   if (fast_dims(d))
     return tc_decode(d, w, q_c, q_r, cache, seq_len, B, max_len, ws, o, as_stream(stream));
   return simt_decode(d, w, q_c, q_r, cache, seq_len, B, max_len, ws, o, as_stream(stream));
+}
+
+mla_status_t mla_project_q_absorbed(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                                    const int32_t* pos, int32_t n, void* ws, size_t ws_bytes,
+                                    void* q_t, void* q_r, void* stream) {
+  MLA_TRY(check_dims(d));
+  if (!w || n < 0) return MLA_ERR_INVALID_ARG;
+  if (!fast_dims(d)) return MLA_ERR_UNSUPPORTED;
+  if (n == 0) return MLA_OK;
+  if (!pos) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_ptr(h));
+  const void* mats[] = {w->W_DQ, w->W_UQ, w->W_QR, w->W_UK};
+  for (const void* p : mats) MLA_TRY(check_ptr(p));
+  MLA_TRY(check_ptr(q_t));
+  MLA_TRY(check_ptr(q_r));
+  size_t need = 0;
+  MLA_TRY(mla_project_q_workspace_size(d, n, &need));
+  if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  MLA_TRY(check_ptr(ws));
+  char* hi = (char*)ws;
+  char* lo = hi + align_up((size_t)n * d->d_cq * 2, 256);
+  MLA_TRY(tc_q_down(d, w, h, n, hi, lo, K_Q_DOWN, as_stream(stream)));
+  return tc_q_absorbed(d, w, hi, lo, pos, n, q_t, q_r, as_stream(stream));
+}
+
+mla_status_t mla_decode_absorbed_latent(const mla_dims_t* d, const mla_weights_t* w,
+                                        const void* q_t, const void* q_r,
+                                        const mla_cache_t* cache, const int32_t* seq_len,
+                                        int32_t B, int32_t max_len, void* ws, size_t ws_bytes,
+                                        float* o, void* stream) {
+  MLA_TRY(check_dims(d));
+  if (!w || !cache || B < 0 || max_len < 0) return MLA_ERR_INVALID_ARG;
+  if (!fast_dims(d)) return MLA_ERR_UNSUPPORTED;
+  if (B == 0) return MLA_OK;
+  if (!seq_len || !cache->seq_base || cache->capacity < 0) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_ptr(q_t));
+  MLA_TRY(check_ptr(q_r));
+  MLA_TRY(check_ptr(w->W_UV));
+  MLA_TRY(check_ptr(o));
+  if (max_len > 0) MLA_TRY(check_ptr(cache->rows));
+  size_t need = 0;
+  MLA_TRY(mla_decode_workspace_size(d, B, max_len, &need));
+  if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  MLA_TRY(check_ptr(ws));
+  return tc_decode_latent(d, w, q_t, q_r, cache, seq_len, B, max_len, ws, o, as_stream(stream));
+}
+
+namespace {
+// Decode-step workspace: the decode workspace (its q~ area holds the absorbed query), then c^Q
+// hi, c^Q lo [B, d_c'] and q^R [B, n_h, d_h^R].
+struct StepLayout {
+  size_t off_hi, off_lo, off_qr, total;
+};
+StepLayout step_layout(const mla_dims_t* d, int B) {
+  StepLayout L;
+  L.off_hi = align_up(tc_decode_ws(d, B), 256);
+  L.off_lo = align_up(L.off_hi + (size_t)B * d->d_cq * 2, 256);
+  L.off_qr = align_up(L.off_lo + (size_t)B * d->d_cq * 2, 256);
+  L.total = align_up(L.off_qr + (size_t)B * d->n_h * d->d_hr * 2, 256);
+  return L;
+}
+}  // namespace
+
+mla_status_t mla_decode_step_workspace_size(const mla_dims_t* d, int32_t B, int32_t max_len,
+                                            size_t* bytes) {
+  MLA_TRY(check_dims(d));
+  if (!bytes || B < 0 || max_len < 0) return MLA_ERR_INVALID_ARG;
+  if (!fast_dims(d)) return MLA_ERR_UNSUPPORTED;
+  *bytes = step_layout(d, B).total;
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_step(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                             const int32_t* pos, mla_cache_t* cache, const int32_t* seq_len,
+                             int32_t B, int32_t max_len, void* ws, size_t ws_bytes, float* o,
+                             void* stream) {
+  MLA_TRY(check_dims(d));
+  if (!w || !cache || B < 0 || max_len < 0) return MLA_ERR_INVALID_ARG;
+  if (!fast_dims(d)) return MLA_ERR_UNSUPPORTED;
+  if (B == 0) return MLA_OK;
+  if (!pos || !seq_len || !cache->seq_base || cache->capacity < 0) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_ptr(h));
+  const void* mats[] = {w->W_DQ, w->W_UQ, w->W_QR, w->W_DKV, w->W_KR, w->W_UK, w->W_UV};
+  for (const void* p : mats) MLA_TRY(check_ptr(p));
+  MLA_TRY(check_ptr(cache->rows));
+  MLA_TRY(check_ptr(o));
+  size_t need = 0;
+  MLA_TRY(mla_decode_step_workspace_size(d, B, max_len, &need));
+  if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
+  MLA_TRY(check_ptr(ws));
+  const StepLayout L = step_layout(d, B);
+  char* wsb = (char*)ws;
+  cudaStream_t st = as_stream(stream);
+  MLA_TRY(tc_down(d, w, h, pos, B, cache, wsb + L.off_hi, wsb + L.off_lo, K_DOWN, st));
+  void* q_t = wsb + tc_decode_qt_offset(B);
+  MLA_TRY(tc_q_absorbed(d, w, wsb + L.off_hi, wsb + L.off_lo, pos, B, q_t, wsb + L.off_qr, st));
+  return tc_decode_latent(d, w, q_t, wsb + L.off_qr, cache, seq_len, B, max_len, ws, o, st);
 }
 
 mla_status_t mla_prefill_workspace_size(const mla_dims_t* d, int32_t n_tok, int32_t B,

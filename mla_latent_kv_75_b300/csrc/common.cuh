@@ -74,10 +74,14 @@ __device__ __forceinline__ float rope_reduce(float pos_part, float fh, float fl)
   return r + a_lo;
 }
 
-__device__ __forceinline__ void rope_cs(int pos, int k, const RopeFreqs& f, float* c, float* s) {
-  const float fh = f.hi[k], fl = f.lo[k];
+// cos and sin of pos * (fh + fl)
+__device__ __forceinline__ void rope_cs_f(int pos, float fh, float fl, float* c, float* s) {
   const float r = rope_reduce((float)(pos & ~4095), fh, fl) + rope_reduce((float)(pos & 4095), fh, fl);
   sincosf(r, s, c);
+}
+
+__device__ __forceinline__ void rope_cs(int pos, int k, const RopeFreqs& f, float* c, float* s) {
+  rope_cs_f(pos, f.hi[k], f.lo[k], c, s);
 }
 
 // ----------------------------------------------------------------------------------

@@ -892,22 +892,29 @@ mla_status_t unabsorb_setup() {
 }  // namespace
 
 size_t tc_decode_ws(const mla_dims_t*, int B) { return layout(B).total; }
+size_t tc_decode_qt_offset(int B) { return layout(B).off_qt; }
 
 mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* q_c,
                        const void* q_r, const mla_cache_t* cache, const int32_t* seq_len, int B,
                        int max_len, void* ws, float* o, cudaStream_t st) {
+  // 1. q~ = (W^UK_i)^T q^C_i into the workspace, then the latent decode
+  void* qt = (char*)ws + layout(B).off_qt;
+  const mla_status_t s = tc_absorb(d, w, q_c, B, qt, K_ABSORB, st);
+  if (s != MLA_OK) return s;
+  return tc_decode_latent(d, w, qt, q_r, cache, seq_len, B, max_len, ws, o, st);
+}
+
+mla_status_t tc_decode_latent(const mla_dims_t* d, const mla_weights_t* w, const void* q_t,
+                              const void* q_r, const mla_cache_t* cache, const int32_t* seq_len,
+                              int B, int max_len, void* ws, float* o, cudaStream_t st) {
   const Layout L = layout(B);
   char* wsb = (char*)ws;
-  __nv_bfloat16* qt = (__nv_bfloat16*)(wsb + L.off_qt);
+  const __nv_bfloat16* qt = (const __nv_bfloat16*)q_t;
   float* part = (float*)(wsb + L.off_part);
   float* ml = (float*)(wsb + L.off_ml);
   int2* rng = (int2*)(wsb + L.off_rng);
   int pairs = 0;
   mla_status_t s = attn_pairs(&pairs);
-  if (s != MLA_OK) return s;
-
-  // 1. q~ = (W^UK_i)^T q^C_i
-  s = tc_absorb(d, w, q_c, B, qt, K_ABSORB, st);
   if (s != MLA_OK) return s;
 
   // 2. attention over the latent cache
@@ -925,7 +932,7 @@ mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* 
       const uint64_t dims[2] = {(uint64_t)kDC, (uint64_t)B * kHeads};
       const uint64_t strides[1] = {(uint64_t)kDC * 2};
       const uint32_t box[2] = {64, (uint32_t)kHeads};
-      if (!make_tmap(&tm_qt, qt, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+      if (!make_tmap(&tm_qt, q_t, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return MLA_ERR_CUDA;
     }
     {
@@ -938,7 +945,7 @@ mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* 
     const float scale_log2 = softmax_scale(d) * 1.4426950408889634f;
     TraceScope ts(K_DECODE_ATTN, st);
     decode_attn_tc_kernel<<<2 * pairs, kThreads, kSmemBytes, st>>>(
-        tm_rows, tm_qt, tm_qr, (const __nv_bfloat16*)qt, seq_len, cache->seq_base,
+        tm_rows, tm_qt, tm_qr, qt, seq_len, cache->seq_base,
         cache->capacity, B, max_len, scale_log2, part, ml, rng);
     s = launch_status();
     if (s != MLA_OK) return s;

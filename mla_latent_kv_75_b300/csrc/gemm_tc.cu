@@ -5,8 +5,10 @@
 // output tile: warp 0 streams 64-wide K slices of W and X into a shared-memory ring with TMA,
 // warp 1 issues tcgen05.mma, warps 2..5 read the accumulator from TMEM and run the epilogue
 // (RoPE on pairs of adjacent output rows, cache-row scatter, dtype conversion).
+#include <map>
 #include <mutex>
 #include <set>
+#include <tuple>
 #include <utility>
 
 #include "internal.h"
@@ -61,9 +63,10 @@ template <int BN, int kMode, bool kDual, int kMaxStages, class Ep>
 __global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow ring: 2 CTAs/SM
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0,
                      const __grid_constant__ CUtensorMap tm_w1,
+                     const __grid_constant__ CUtensorMap tm_w2,
                      const __grid_constant__ CUtensorMap tm_x,
-                     const __grid_constant__ CUtensorMap tm_x2, int m_tiles0, int O, int N,
-                     int k_chunks, int mt_group, int mt_cta, int C, Ep ep) {
+                     const __grid_constant__ CUtensorMap tm_x2, int m_tiles0, int m_tiles01,
+                     int O, int N, int k_chunks, int mt_group, int mt_cta, int C, Ep ep) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -124,9 +127,10 @@ __global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow
       mbar_arrive_expect_tx(&full[s], S::kStage);
       const int kx = kc * 64;
       if (kMode == kPlain) {
-        const bool from_w1 = m_tile >= m_tiles0;
-        tma_load_2d(a, from_w1 ? &tm_w1 : &tm_w0, &full[s], kx,
-                    (from_w1 ? m_tile - m_tiles0 : m_tile) * 128);
+        // m-tiles [0, m_tiles0) come from W0, [m_tiles0, m_tiles01) from W1, the rest from W2
+        const int w_sel = m_tile < m_tiles0 ? 0 : (m_tile < m_tiles01 ? 1 : 2);
+        const int w_row = (m_tile - (w_sel == 0 ? 0 : (w_sel == 1 ? m_tiles0 : m_tiles01))) * 128;
+        tma_load_2d(a, w_sel == 0 ? &tm_w0 : (w_sel == 1 ? &tm_w1 : &tm_w2), &full[s], kx, w_row);
         tma_load_2d(b, &tm_x, &full[s], kx, n0);
         if (kDual) tma_load_2d(b + S::kTileB, &tm_x2, &full[s], kx, n0);
       } else {
@@ -199,12 +203,10 @@ __global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow
             for (int j = 0; j < 32; ++j) v[j] += v2[j];
           }
           tmem_wait_ld();
+          float vp[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float vp = __shfl_xor_sync(0xffffffffu, v[j], 1);
-            const int n = n0 + c + j;
-            if (n < N && o < O) ep(o, n, v[j], vp);
-          }
+          for (int j = 0; j < 32; ++j) vp[j] = __shfl_xor_sync(0xffffffffu, v[j], 1);
+          if (o < O) ep.row32(o, n0 + c, N, v, vp);
         }
       }
     }
@@ -268,9 +270,14 @@ __global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow
 // Persistent variant of the plain-mode GEMM for many output tiles (prefill-sized N): one CTA
 // per SM walks tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... (m-tile fastest, so that the
 // CTAs in flight share one activation tile), the TMA ring runs on across tile boundaries, and
-// two TMEM accumulators let the epilogue of one tile overlap the MMAs of the next.
+// two TMEM accumulators let the epilogue of one tile overlap the MMAs of the next. The epilogue
+// (bf16 conversion, RoPE, scattered stores) takes as long as the MMAs at these sizes, so eight
+// warps run it: two per TMEM lane quarter, each on half of the tile's columns.
+constexpr int kPThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kPEpiWarps = 8;
+
 template <int BN, bool kDual, class Ep>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kPThreads, 1)
     proj_gemm_persistent(const __grid_constant__ CUtensorMap tm_w0,
                          const __grid_constant__ CUtensorMap tm_w1,
                          const __grid_constant__ CUtensorMap tm_x,
@@ -303,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], kPEpiWarps);
     }
     mbar_init(mma_done, 1);
     *abort = 0;
@@ -389,6 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 2) {
     // ---------------- epilogue: TMEM -> registers -> global, overlapped with the next tile
     const int q = warp & 3;
+    constexpr int kWarpCols = BN >= 64 ? BN / 2 : BN;  // columns per epilogue warp
+    const int c_beg = ((warp - 2) >> 2) * kWarpCols;
     for (int i = 0; i < my_tiles; ++i) {
       const int buf = i & 1;
       const int t = blockIdx.x + i * gridDim.x;
@@ -397,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int o = m_tile * 128 + q * 32 + lane;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
+      for (int c = c_beg; c < c_beg + kWarpCols && c < BN; c += 32) {
         float v[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * kAccN + c, v);
         if (kDual) {
@@ -408,12 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j) v[j] += v2[j];
         }
         tmem_wait_ld();
+        float vp[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float vp = __shfl_xor_sync(0xffffffffu, v[j], 1);
-          const int n = n0 + c + j;
-          if (n < N && o < O) ep(o, n, v[j], vp);
-        }
+        for (int j = 0; j < 32; ++j) vp[j] = __shfl_xor_sync(0xffffffffu, v[j], 1);
+        if (o < O) ep.row32(o, n0 + c, N, v, vp);
       }
       tc_fence_before();
       __syncwarp();
@@ -429,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------------- epilogues
 // Cache append: rows [0, d_c) of [W^DKV; W^KR] are c^KV, rows [d_c, d_c + d_hr) are k^R,
-// rotated by RoPE at the token's position. Optionally also stored to a packed copy.
+// rotated by RoPE at the token's position. Optionally also stored to a packed copy. Token n
+// belongs to sequence seq_idx[n], or to sequence n when seq_idx is null (a decode step).
 struct EpAppend {
   __nv_bfloat16* rows;
   int64_t pitch, capacity;
@@ -447,13 +455,38 @@ struct EpAppend {
       v = ((o - d_c) & 1) ? (vp * s + v * c) : (v * c - vp * s);
     }
     const __nv_bfloat16 b = __float2bfloat16_rn(v);
-    const int64_t row = seq_base[seq_idx[n]] + p;
+    const int64_t row = seq_base[seq_idx ? seq_idx[n] : n] + p;
     if (row < 0 || row >= capacity) {
       flag_status(MLA_ERR_CAPACITY);
     } else {
       rows[row * pitch + o] = b;
     }
     if (packed) packed[(int64_t)n * pitch + o] = b;
+  }
+  // output row o for tokens nb .. nb+31 (those below N); vp holds the partner rows' values
+  __device__ void row32(int o, int nb, int N, const float* v, const float* vp) const {
+    const bool rot = o >= d_c;
+    const int e = o - d_c;
+    const float fh = rot ? rf.hi[e >> 1] : 0.f, fl = rot ? rf.lo[e >> 1] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int n = nb + j;
+      if (n >= N) break;
+      const int p = pos[n];
+      float x = v[j];
+      if (rot) {
+        float c, s;
+        rope_cs_f(p, fh, fl, &c, &s);
+        x = (e & 1) ? (vp[j] * s + x * c) : (x * c - vp[j] * s);
+      }
+      const __nv_bfloat16 b = __float2bfloat16_rn(x);
+      const int64_t row = seq_base[seq_idx ? seq_idx[n] : n] + p;
+      if (row < 0 || row >= capacity)
+        flag_status(MLA_ERR_CAPACITY);
+      else
+        rows[row * pitch + o] = b;
+      if (packed) packed[(int64_t)n * pitch + o] = b;
+    }
   }
 };
 
@@ -466,6 +499,55 @@ struct EpStoreBF16 {
     const __nv_bfloat16 h = __float2bfloat16_rn(v);
     hi[(int64_t)n * ld + o] = h;
     if (lo) lo[(int64_t)n * ld + o] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+  __device__ void row32(int o, int nb, int N, const float* v, const float*) const {
+    __nv_bfloat16* ph = hi + (int64_t)nb * ld + o;
+    __nv_bfloat16* pl = lo ? lo + (int64_t)nb * ld + o : nullptr;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (nb + j >= N) break;
+      const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
+      ph[(int64_t)j * ld] = h;
+      if (pl) pl[(int64_t)j * ld] = __float2bfloat16_rn(v[j] - __bfloat162float(h));
+    }
+  }
+};
+
+// Plain store Y[n * ld + o] in fp16.
+struct EpStoreF16 {
+  __half* y;
+  int64_t ld;
+  __device__ void operator()(int o, int n, float v, float) const {
+    y[(int64_t)n * ld + o] = __float2half_rn(v);
+  }
+  __device__ void row32(int o, int nb, int N, const float* v, const float*) const {
+    __half* p = y + (int64_t)nb * ld + o;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (nb + j >= N) break;
+      p[(int64_t)j * ld] = __float2half_rn(v[j]);
+    }
+  }
+};
+
+// Down-projections of a decode step in one GEMM over [W^DKV; W^KR; W^DQ]: output rows
+// [0, d_c + d_hr) are the cache row (EpAppend), rows from q_row0 on are c^Q as a hi/lo pair;
+// the rows between (the padding of W^KR's tile) are dropped.
+struct EpDown {
+  EpAppend app;
+  EpStoreBF16 cq;
+  int row_end, q_row0;
+  __device__ void operator()(int o, int n, float v, float vp) const {
+    if (o < row_end)
+      app(o, n, v, vp);
+    else if (o >= q_row0)
+      cq(o - q_row0, n, v, vp);
+  }
+  __device__ void row32(int o, int nb, int N, const float* v, const float* vp) const {
+    if (o < row_end)
+      app.row32(o, nb, N, v, vp);
+    else if (o >= q_row0)
+      cq.row32(o - q_row0, nb, N, v, vp);
   }
 };
 
@@ -490,6 +572,31 @@ struct EpQuery {
       rope_cs(pos[n], e >> 1, rf, &c, &s);
       v = (e & 1) ? (vp * s + v * c) : (v * c - vp * s);
       q_r[n * qr_tok + i * qr_head + e] = from_f<T>(v);
+    }
+  }
+  // output row o for tokens nb .. nb+31: the head split, the destination and the RoPE frequency
+  // are worked out once per row
+  __device__ void row32(int o, int nb, int N, const float* v, const float* vp) const {
+    const int nc = n_h * d_hc;
+    if (o < nc) {
+      T* dst = q_c + (int64_t)nb * qc_tok + (o / d_hc) * qc_head + (o % d_hc);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (nb + j >= N) break;
+        dst[(int64_t)j * qc_tok] = from_f<T>(v[j]);
+      }
+    } else {
+      const int r = o - nc, i = r / d_hr, e = r % d_hr;
+      const float fh = rf.hi[e >> 1], fl = rf.lo[e >> 1];
+      T* dst = q_r + (int64_t)nb * qr_tok + i * qr_head + e;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (nb + j >= N) break;
+        float c, s;
+        rope_cs_f(pos[nb + j], fh, fl, &c, &s);
+        const float x = (e & 1) ? (vp[j] * s + v[j] * c) : (v[j] * c - vp[j] * s);
+        dst[(int64_t)j * qr_tok] = from_f<T>(x);
+      }
     }
   }
 };
@@ -522,24 +629,57 @@ int sm_count() {
   return n;
 }
 
-// Split-K cluster size: the largest power of two <= kMaxCluster that keeps the grid within one
-// wave of the SMs and leaves every cluster rank at least one K chunk.
-int choose_split(int tiles, int k_chunks) {
+// Clusters of `c` CTAs of kernel `fn` (with `smem` bytes each) that the device holds at once,
+// cached per (kernel, size, device); 0 if the query fails.
+int max_active_clusters(const void* fn, int c, int smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int>, int> known;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(fn, c, dev);
+  auto it = known.find(key);
+  if (it != known.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  known[key] = n;
+  return n;
+}
+
+// Split-K cluster size: the largest power of two <= kMaxCluster whose clusters (one per output
+// tile) are all resident at once, so the grid runs as one wave, and that leaves every cluster
+// rank at least one K chunk.
+int choose_split(int tiles, int k_chunks, const void* fn, int smem) {
   const int sms = sm_count();
   int c = 1;
   for (int n = 2; n <= kMaxCluster && tiles * n <= sms; n *= 2) {
     const int per = (k_chunks + n - 1) / n;
     if (per * (n - 1) >= k_chunks) break;  // the last rank would get no K chunk
+    if (max_active_clusters(fn, n, smem) < tiles) break;
     c = n;
   }
   return c;
 }
 
 template <int BN, int kMode, bool kDual, int kMaxStages = 8, class Ep>
-mla_status_t launch_kernel(const CUtensorMap& tw0, const CUtensorMap& tw1, const CUtensorMap& tx,
-                           const CUtensorMap& tx2, int m_tiles0, int O, int N, int k_chunks,
-                           int mt_group, int mt_cta, int C, int grid_x, int kid, const Ep& ep,
-                           cudaStream_t st) {
+mla_status_t launch_kernel(const CUtensorMap& tw0, const CUtensorMap& tw1, const CUtensorMap& tw2,
+                           const CUtensorMap& tx, const CUtensorMap& tx2, int m_tiles0,
+                           int m_tiles01, int O, int N, int k_chunks, int mt_group, int mt_cta,
+                           int C, int grid_x, int kid, const Ep& ep, cudaStream_t st) {
   const uint32_t smem = ProjSmem<BN, kDual, kMaxStages>::kBytes + 1024;
   auto kern = proj_gemm_kernel<BN, kMode, kDual, kMaxStages, Ep>;
   mla_status_t s = ensure_smem((const void*)kern, (int)smem);
@@ -557,8 +697,8 @@ mla_status_t launch_kernel(const CUtensorMap& tw0, const CUtensorMap& tw1, const
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   TraceScope ts(kid, st);
-  if (cudaLaunchKernelEx(&cfg, kern, tw0, tw1, tx, tx2, m_tiles0, O, N, k_chunks, mt_group,
-                         mt_cta, C, ep) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, kern, tw0, tw1, tw2, tx, tx2, m_tiles0, m_tiles01, O, N, k_chunks,
+                         mt_group, mt_cta, C, ep) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }
@@ -575,23 +715,42 @@ mla_status_t launch_persistent(const CUtensorMap& tw0, const CUtensorMap& tw1,
   const int n_tiles = ceil_div(N, BN);
   const int grid = min(sm_count(), m_tiles * n_tiles);
   TraceScope ts(kid, st);
-  kern<<<grid, kThreads, smem, st>>>(tw0, tw1, tx, tx2, m_tiles0, m_tiles, n_tiles, O, N,
-                                     k_chunks, ep);
+  kern<<<grid, kPThreads, smem, st>>>(tw0, tw1, tx, tx2, m_tiles0, m_tiles, n_tiles, O, N,
+                                      k_chunks, ep);
   return launch_status();
 }
 
 template <int BN, class Ep>
 mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
-  CUtensorMap tw0, tw1, tx, tx2;
+  CUtensorMap tw0, tw1, tw2, tx, tx2;
   const int m0 = a.O0 / 128;
   if (!tmap_rows(&tw0, a.W0, a.O0, a.K, a.K, 128)) return MLA_ERR_CUDA;
   if (!tmap_rows(&tw1, a.W1 ? a.W1 : a.W0, a.W1 ? a.O1 : a.O0, a.K, a.K, 128)) return MLA_ERR_CUDA;
+  if (!tmap_rows(&tw2, a.W2 ? a.W2 : a.W0, a.W2 ? a.O2 : a.O0, a.K, a.K, 128)) return MLA_ERR_CUDA;
   if (!tmap_rows(&tx, a.X, a.N, a.K, a.ldx, BN)) return MLA_ERR_CUDA;
   if (!tmap_rows(&tx2, a.X2 ? a.X2 : a.X, a.N, a.K, a.ldx, BN)) return MLA_ERR_CUDA;
-  const int m_tiles = m0 + (a.W1 ? ceil_div(a.O1, 128) : 0);
+  // a W1 block that is not a multiple of 128 rows is padded to whole tiles (rows read past it
+  // are zero), so W2's rows start at output row (m0 + ceil(O1 / 128)) * 128
+  const int m01 = m0 + (a.W1 ? ceil_div(a.O1, 128) : 0);
+  const int m_tiles = m01 + (a.W2 ? ceil_div(a.O2, 128) : 0);
   const int k_chunks = a.K / 64;
-  const int C = choose_split(m_tiles * ceil_div(a.N, BN), k_chunks);
-  const int O = a.O0 + (a.W1 ? a.O1 : 0);
+  // split-K kernel of this launch (cluster size chosen against its residency)
+  const void* split_fn = (const void*)proj_gemm_kernel<BN, kPlain, false, 8, Ep>;
+  int split_smem = (int)ProjSmem<BN, false>::kBytes + 1024;
+  if constexpr (BN <= 128) {  // hi/lo inputs need MMAs of width 2*BN
+    if (a.X2) {
+      split_fn = (const void*)proj_gemm_kernel<BN, kPlain, true, 8, Ep>;
+      split_smem = (int)ProjSmem<BN, true>::kBytes + 1024;
+    }
+  }
+  int C = 1;
+  if (m_tiles * ceil_div(a.N, BN) * 2 <= sm_count()) {
+    mla_status_t es = ensure_smem(split_fn, split_smem);
+    if (es != MLA_OK) return es;
+    C = choose_split(m_tiles * ceil_div(a.N, BN), k_chunks, split_fn, split_smem);
+  }
+  const int O = a.W2 ? m01 * 128 + a.O2 : a.O0 + (a.W1 ? a.O1 : 0);
+  if (a.W2 && m_tiles * ceil_div(a.N, BN) > sm_count()) return MLA_ERR_UNSUPPORTED;
   if (m_tiles * ceil_div(a.N, BN) > sm_count()) {
     if constexpr (BN == 32)
       if (m_tiles <= 2 * sm_count()) {
@@ -599,10 +758,10 @@ mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
         // share an SM, so every m-tile streams its weights at once in a single wave instead of
         // a persistent CTA walking a second tile after the others have finished.
         if (a.X2)
-          return launch_kernel<BN, kPlain, true, 4>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1,
-                                                    1, 1, m_tiles, a.kid, ep, st);
-        return launch_kernel<BN, kPlain, false, 4>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1, 1,
-                                                   1, m_tiles, a.kid, ep, st);
+          return launch_kernel<BN, kPlain, true, 4>(tw0, tw1, tw2, tx, tx2, m0, m01, O, a.N,
+                                                    k_chunks, 1, 1, 1, m_tiles, a.kid, ep, st);
+        return launch_kernel<BN, kPlain, false, 4>(tw0, tw1, tw2, tx, tx2, m0, m01, O, a.N,
+                                                   k_chunks, 1, 1, 1, m_tiles, a.kid, ep, st);
       }
     if (a.X2) {
       if constexpr (BN <= 128)  // two accumulators of width 2*BN must fit in tensor memory
@@ -616,13 +775,13 @@ mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
   }
   if (a.X2) {
     if constexpr (BN <= 128)  // one MMA covers both halves: 2*BN columns, at most 256
-      return launch_kernel<BN, kPlain, true>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1, 1, C,
-                                             m_tiles * C, a.kid, ep, st);
+      return launch_kernel<BN, kPlain, true>(tw0, tw1, tw2, tx, tx2, m0, m01, O, a.N, k_chunks, 1,
+                                             1, C, m_tiles * C, a.kid, ep, st);
     else
       return MLA_ERR_UNSUPPORTED;
   }
-  return launch_kernel<BN, kPlain, false>(tw0, tw1, tx, tx2, m0, O, a.N, k_chunks, 1, 1, C,
-                                          m_tiles * C, a.kid, ep, st);
+  return launch_kernel<BN, kPlain, false>(tw0, tw1, tw2, tx, tx2, m0, m01, O, a.N, k_chunks, 1, 1,
+                                          C, m_tiles * C, a.kid, ep, st);
 }
 
 template <class Ep>
@@ -681,18 +840,21 @@ mla_status_t launch_grouped_bn(const GroupArgs& a, const Ep& ep, cudaStream_t st
              m_tiles * 2 * C <= 2 * sms)
         C *= 2;
     const int grid_x = (m_tiles / mtc) * C;
-    return launch_kernel<BN, kMode, false, 4>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, k_chunks,
-                                              mt_group, mtc, C, grid_x, a.kid, ep, st);
+    return launch_kernel<BN, kMode, false, 4>(tw, tw, tw, tx, tx2, m_tiles, m_tiles, a.G * a.Mg,
+                                              a.N, k_chunks, mt_group, mtc, C, grid_x, a.kid, ep,
+                                              st);
   }
   if (a.X2) {
     if constexpr (BN <= 128)  // one MMA covers both halves: 2*BN columns, at most 256
-      return launch_kernel<BN, kMode, true>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, k_chunks,
-                                            mt_group, mt_cta, 1, m_tiles / mt_cta, a.kid, ep, st);
+      return launch_kernel<BN, kMode, true>(tw, tw, tw, tx, tx2, m_tiles, m_tiles, a.G * a.Mg, a.N,
+                                            k_chunks, mt_group, mt_cta, 1, m_tiles / mt_cta, a.kid,
+                                            ep, st);
     else
       return MLA_ERR_UNSUPPORTED;
   }
-  return launch_kernel<BN, kMode, false>(tw, tw, tx, tx2, m_tiles, a.G * a.Mg, a.N, k_chunks,
-                                         mt_group, mt_cta, 1, m_tiles / mt_cta, a.kid, ep, st);
+  return launch_kernel<BN, kMode, false>(tw, tw, tw, tx, tx2, m_tiles, m_tiles, a.G * a.Mg, a.N,
+                                         k_chunks, mt_group, mt_cta, 1, m_tiles / mt_cta, a.kid, ep,
+                                         st);
 }
 
 template <int kMode, class Ep>
@@ -726,6 +888,31 @@ mla_status_t tc_append(const mla_dims_t* d, const mla_weights_t* w, const void* 
   return launch_proj(a, ep, st);
 }
 
+// Append + c^Q of a decode step ("MLA前向计算流程" §三分支计算 ①②③): token n of h is sequence
+// n's token at position pos[n]; one launch streams W^DKV, W^KR and W^DQ once.
+mla_status_t tc_down(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                     const int32_t* pos, int n, mla_cache_t* cache, void* cq_hi, void* cq_lo,
+                     int kid, cudaStream_t st) {
+  ProjArgs a{};
+  a.W0 = w->W_DKV;
+  a.O0 = d->d_c;
+  a.W1 = w->W_KR;
+  a.O1 = d->d_hr;
+  a.W2 = w->W_DQ;
+  a.O2 = d->d_cq;
+  a.K = d->d;
+  a.X = h;
+  a.ldx = d->d;
+  a.N = n;
+  a.kid = kid;
+  const int q_row0 = (d->d_c / 128 + ceil_div(d->d_hr, 128)) * 128;
+  EpDown ep{EpAppend{(__nv_bfloat16*)cache->rows, (int64_t)(d->d_c + d->d_hr), cache->capacity,
+                     cache->seq_base, nullptr, pos, nullptr, d->d_c, rope_freqs(d)},
+            EpStoreBF16{(__nv_bfloat16*)cq_hi, (__nv_bfloat16*)cq_lo, d->d_cq},
+            d->d_c + d->d_hr, q_row0};
+  return launch_proj(a, ep, st);
+}
+
 mla_status_t tc_q_down(const mla_dims_t* d, const mla_weights_t* w, const void* h, int n,
                        void* cq_hi, void* cq_lo, int kid, cudaStream_t st) {
   ProjArgs a{};
@@ -751,7 +938,7 @@ mla_status_t tc_q_up(const mla_dims_t* d, const mla_weights_t* w, const void* cq
   a.O1 = d->n_h * d->d_hr;
   a.K = d->d_cq;
   a.X = cq_hi;
-  a.X2 = cq_lo;
+  a.X2 = cq_lo;  // null: c^Q as a single bf16 operand
   a.ldx = d->d_cq;
   a.N = n;
   a.kid = kid;
@@ -766,7 +953,7 @@ mla_status_t tc_q_up(const mla_dims_t* d, const mla_weights_t* w, const void* cq
 }
 
 mla_status_t tc_expand(const void* W, int O, const void* latent, int64_t ld_latent, int K, int n,
-                       void* y, int kid, cudaStream_t st) {
+                       void* y, bool f16_out, int kid, cudaStream_t st) {
   ProjArgs a{};
   a.W0 = W;
   a.O0 = O;
@@ -775,6 +962,10 @@ mla_status_t tc_expand(const void* W, int O, const void* latent, int64_t ld_late
   a.ldx = ld_latent;
   a.N = n;
   a.kid = kid;
+  if (f16_out) {
+    EpStoreF16 ep{(__half*)y, O};
+    return launch_proj(a, ep, st);
+  }
   EpStoreBF16 ep{(__nv_bfloat16*)y, nullptr, O};
   return launch_proj(a, ep, st);
 }

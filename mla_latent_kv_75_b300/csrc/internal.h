@@ -11,7 +11,7 @@ namespace mla {
 enum KernelId : int {
   K_APPEND = 0, K_Q_DOWN, K_Q_UP, K_ABSORB, K_DECODE_ATTN, K_DECODE_COMBINE, K_TOKEN_MAP,
   K_PREFILL_APPEND, K_PREFILL_Q_DOWN, K_PREFILL_Q_UP, K_EXPAND_K, K_EXPAND_V, K_PREFILL_ATTN,
-  K_DECODE_MERGE, K_UNABSORB, K_NUM_IDS
+  K_DECODE_MERGE, K_UNABSORB, K_Q_ABSORB, K_DOWN, K_NUM_IDS
 };
 
 // Launch tracing (host side): while armed, trace_before/trace_after record caller-owned
@@ -50,6 +50,9 @@ bool fast_dims(const mla_dims_t* d);
 mla_status_t tc_append(const mla_dims_t* d, const mla_weights_t* w, const void* h,
                        const int32_t* seq_idx, const int32_t* pos, int n, mla_cache_t* cache,
                        void* packed, int kid, cudaStream_t st);
+mla_status_t tc_down(const mla_dims_t* d, const mla_weights_t* w, const void* h,
+                     const int32_t* pos, int n, mla_cache_t* cache, void* cq_hi, void* cq_lo,
+                     int kid, cudaStream_t st);
 mla_status_t tc_q_down(const mla_dims_t* d, const mla_weights_t* w, const void* h, int n,
                        void* cq_hi, void* cq_lo, int kid, cudaStream_t st);
 mla_status_t tc_q_up(const mla_dims_t* d, const mla_weights_t* w, const void* cq_hi,
@@ -59,6 +62,11 @@ mla_status_t tc_q_up(const mla_dims_t* d, const mla_weights_t* w, const void* cq
 mla_status_t tc_absorb(const mla_dims_t* d, const mla_weights_t* w, const void* q_c, int B,
                        void* qt, int kid, cudaStream_t st);
 
+// Fused query up-projection + absorption (V2 widths, bf16): qabsorb_tc.cu
+mla_status_t tc_q_absorbed(const mla_dims_t* d, const mla_weights_t* w, const void* cq_hi,
+                           const void* cq_lo, const int32_t* pos, int n, void* q_t, void* q_r,
+                           cudaStream_t st);
+
 // Tensor-core causal prefill (V2 widths, bf16): prefill_tc.cu
 size_t tc_prefill_ws(const mla_dims_t* d, int n_tok);
 mla_status_t tc_prefill(const mla_dims_t* d, const mla_weights_t* w, const void* h,
@@ -67,10 +75,15 @@ mla_status_t tc_prefill(const mla_dims_t* d, const mla_weights_t* w, const void*
 
 // Tensor-core absorbed decode (V2 widths, bf16): decode_tc.cu
 size_t tc_decode_ws(const mla_dims_t* d, int B);
+size_t tc_decode_qt_offset(int B);  // byte offset of the q~ area in the decode workspace
 mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* q_c,
                        const void* q_r, const mla_cache_t* cache, const int32_t* seq_len, int B,
                        int max_len, void* ws, float* o, cudaStream_t st);
+// Decode from the absorbed query q~ [B, n_h, d_c] (attention + merge + W^UV): no absorb launch.
+mla_status_t tc_decode_latent(const mla_dims_t* d, const mla_weights_t* w, const void* q_t,
+                              const void* q_r, const mla_cache_t* cache, const int32_t* seq_len,
+                              int B, int max_len, void* ws, float* o, cudaStream_t st);
 mla_status_t tc_expand(const void* W, int O, const void* latent, int64_t ld_latent, int K, int n,
-                       void* y, int kid, cudaStream_t st);
+                       void* y, bool f16_out, int kid, cudaStream_t st);
 
 }  // namespace mla

@@ -7,8 +7,10 @@
 //
 // Launch sequence (all tcgen05 kernels except the token map):
 //   token map  -> append (cache rows + a packed copy of the latent rows)
-//   -> c^Q (hi/lo bf16) -> [q^C ; q^R] per head (bf16, RoPE in the epilogue)
-//   -> K^C = W^UK c and V = W^UV c per head (bf16) -> causal attention (this file).
+//   -> c^Q (bf16) -> [q^C ; q^R] per head (bf16, RoPE in the epilogue)
+//   -> K^C = W^UK c (bf16) and V = W^UV c (fp16) per head -> causal attention (this file).
+// P and V meet in fp16 (P in [0, 2^8] under the lazy rescale): the rounding of P and V sets this
+// path's error, and fp16 keeps three more bits than bf16 at the same MMA rate.
 //
 // Attention kernel: one CTA per (128-query tile, head, sequence). Blocks are dispatched with all
 // query tiles of a head together (heaviest first), so the K/V tiles they share stay in L2.
@@ -56,15 +58,17 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 4096, "barrier block");
 
+// Two probabilities as an fp16 pair (P in [0, 2^8] with the lazy rescale; fp16 keeps 3 more
+// mantissa bits than bf16, and V is stored in fp16 to match).
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  const __half2 v = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,   // Q  [n, 128, 192]
                            const __grid_constant__ CUtensorMap tm_kc,  // K^C [n, 128, 128]
-                           const __grid_constant__ CUtensorMap tm_v,   // V  [n, 128, 128]
+                           const __grid_constant__ CUtensorMap tm_v,   // V  [n, 128, 128] fp16
                            const __grid_constant__ CUtensorMap tm_kr,  // latent rows [n, 576]
                            const int32_t* __restrict__ cu, float scale_log2,
                            float* __restrict__ o) {
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc_s = idesc_f16(128, kBK, 1, 0, 0);  // A, B K-major
-    constexpr uint32_t idesc_o = idesc_f16(128, kDV, 1, 0, 1);  // B (V) MN-major
+    constexpr uint32_t idesc_o = idesc_f16(128, kDV, 0, 0, 1);  // fp16 P and V; V MN-major
     const uint64_t desc_q = smem_desc(smem_u32(smem + kOffQ), 16, 1024);
     const uint64_t desc_k = smem_desc(smem_u32(smem + kOffK), 16, 1024);
     const uint64_t desc_v = smem_desc(smem_u32(smem + kOffV), kBox, 1024);
@@ -236,7 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float p0 = ex2(fmaf(sc[2 * k], scale_log2, -base));
         const float p1 = ex2(fmaf(sc[2 * k + 1], scale_log2, -base));
         w[k] = pack2(p0, p1);
-        ls[k & 3] += p0 + p1;
+        // the row sum is of the rounded P, so the normalisation matches what PV multiplies
+        const __half2 pr = *reinterpret_cast<const __half2*>(&w[k]);
+        ls[k & 3] += __low2float(pr) + __high2float(pr);
       }
       tmem_st32u(lane_base + s * 128 + half * 32, w);
       l_half = l_half * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
@@ -309,7 +315,7 @@ __global__ void prefill_token_map_kernel(const int32_t* __restrict__ cu, int B, 
 }
 
 struct Layout {
-  size_t off_seq, off_pos, off_lat, off_hi, off_lo, off_q, off_kc, off_v, total;
+  size_t off_seq, off_pos, off_lat, off_hi, off_q, off_kc, off_v, total;
 };
 
 Layout layout(const mla_dims_t* d, int n) {
@@ -318,8 +324,7 @@ Layout layout(const mla_dims_t* d, int n) {
   L.off_pos = align_up(L.off_seq + (size_t)n * 4, 256);
   L.off_lat = align_up(L.off_pos + (size_t)n * 4, 256);
   L.off_hi = align_up(L.off_lat + (size_t)n * kRow * 2, 256);
-  L.off_lo = align_up(L.off_hi + (size_t)n * d->d_cq * 2, 256);
-  L.off_q = align_up(L.off_lo + (size_t)n * d->d_cq * 2, 256);
+  L.off_q = align_up(L.off_hi + (size_t)n * d->d_cq * 2, 256);
   L.off_kc = align_up(L.off_q + (size_t)n * kH * kDQK * 2, 256);
   L.off_v = align_up(L.off_kc + (size_t)n * kH * kDV * 2, 256);
   L.total = align_up(L.off_v + (size_t)n * kH * kDV * 2, 256);
@@ -347,7 +352,6 @@ mla_status_t tc_prefill(const mla_dims_t* d, const mla_weights_t* w, const void*
   int32_t* tpos = (int32_t*)(wsb + L.off_pos);
   void* lat = wsb + L.off_lat;
   void* cq_hi = wsb + L.off_hi;
-  void* cq_lo = wsb + L.off_lo;
   __nv_bfloat16* Q = (__nv_bfloat16*)(wsb + L.off_q);
   void* KC = wsb + L.off_kc;
   void* V = wsb + L.off_v;
@@ -361,15 +365,16 @@ mla_status_t tc_prefill(const mla_dims_t* d, const mla_weights_t* w, const void*
   s = tc_append(d, w, h, tseq, tpos, n, cache, lat, K_PREFILL_APPEND, st);
   if (s != MLA_OK) return s;
   // queries: c^Q, then [q^C ; q^R] per head, interleaved [n, n_h, 192]
-  s = tc_q_down(d, w, h, n, cq_hi, cq_lo, K_PREFILL_Q_DOWN, st);
+  // c^Q as one bf16 operand (the error budget of the path is set by P and V, kept in fp16)
+  s = tc_q_down(d, w, h, n, cq_hi, nullptr, K_PREFILL_Q_DOWN, st);
   if (s != MLA_OK) return s;
-  s = tc_q_up(d, w, cq_hi, cq_lo, tpos, n, Q, Q + d->d_hc, (int64_t)kH * kDQK, kDQK,
+  s = tc_q_up(d, w, cq_hi, nullptr, tpos, n, Q, Q + d->d_hc, (int64_t)kH * kDQK, kDQK,
               (int64_t)kH * kDQK, kDQK, false, K_PREFILL_Q_UP, st);
   if (s != MLA_OK) return s;
   // K^C and V per head from the latent rows
-  s = tc_expand(w->W_UK, kH * kDV, lat, kRow, kDC, n, KC, K_EXPAND_K, st);
+  s = tc_expand(w->W_UK, kH * kDV, lat, kRow, kDC, n, KC, false, K_EXPAND_K, st);
   if (s != MLA_OK) return s;
-  s = tc_expand(w->W_UV, kH * kDV, lat, kRow, kDC, n, V, K_EXPAND_V, st);
+  s = tc_expand(w->W_UV, kH * kDV, lat, kRow, kDC, n, V, true, K_EXPAND_V, st);  // fp16
   if (s != MLA_OK) return s;
   // causal attention
   CUtensorMap tq, tkc, tv, tkr;

@@ -11,8 +11,9 @@ import numpy as np
 import torch
 
 from . import (MLA_BF16, MLA_F32, make_cache, make_dims, make_weights, mla_append_cache,
-               mla_decode_absorbed, mla_decode_workspace_size, mla_prefill,
-               mla_prefill_workspace_size, mla_project_q, mla_project_q_workspace_size)
+               mla_decode_absorbed, mla_decode_step, mla_decode_step_workspace_size,
+               mla_decode_workspace_size, mla_fast_path, mla_prefill, mla_prefill_workspace_size,
+               mla_project_q, mla_project_q_workspace_size)
 
 WEIGHT_NAMES = ("W_DQ", "W_UQ", "W_QR", "W_DKV", "W_KR", "W_UK", "W_UV")
 
@@ -103,10 +104,13 @@ def fill_context(model: DeviceModel, cache: LatentCache, hidden_fn, seq_lens: Se
 
 class DecodeStep:
     """Buffers and calls of one decode step: append the new tokens' rows, project their
-    queries, run absorbed decode over ``seq_len`` rows per sequence."""
+    queries, run absorbed decode over ``seq_len`` rows per sequence. ``fused`` (tensor-core
+    dims only) runs the step as the single mla_decode_step call (down-projections in one
+    launch, query up-projection fused with the absorption); otherwise as the three calls
+    mla_append_cache, mla_project_q and mla_decode_absorbed."""
 
     def __init__(self, model: DeviceModel, cache: LatentCache, seq_lens: Sequence[int],
-                 max_len: Optional[int] = None):
+                 max_len: Optional[int] = None, fused: bool = False):
         dev = cache.rows.device
         d = model.dims
         self.model, self.cache = model, cache
@@ -125,6 +129,10 @@ class DecodeStep:
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self._dims, self._w = model.abi_dims, model.abi_weights
         self._cache = cache.abi
+        self.fused = bool(fused) and mla_fast_path(self._dims) == 1
+        if self.fused:
+            self.step_ws_bytes = mla_decode_step_workspace_size(self._dims, self.B, self.max_len)
+            self.step_ws = torch.empty(max(self.step_ws_bytes, 256), dtype=torch.uint8, device=dev)
 
     def append(self, h_new: torch.Tensor, stream=None) -> None:
         mla_append_cache(self._dims, self._w, h_new, self.seq_idx, self.pos, self.B, self._cache,
@@ -141,6 +149,10 @@ class DecodeStep:
         return self.o
 
     def step(self, h_new: torch.Tensor, stream=None) -> torch.Tensor:
+        if self.fused:
+            mla_decode_step(self._dims, self._w, h_new, self.pos, self._cache, self.seq_len,
+                            self.B, self.max_len, self.step_ws, self.step_ws_bytes, self.o, stream)
+            return self.o
         self.append(h_new, stream)
         self.project(h_new, stream)
         return self.decode(stream)
