@@ -222,6 +222,16 @@ mla_status_t mla_prefill(const mla_dims_t* dims, const mla_weights_t* w, const v
  * flagged anything), or MLA_ERR_CUDA if the stream reports a CUDA error. */
 mla_status_t mla_get_device_status(void* stream);
 
+/* Test hook for the bounded device waits (no counterpart on the pages). Arms a one-shot: the
+ * next tensor-core decode attention launch (mla_decode_absorbed, mla_decode_absorbed_latent,
+ * mla_decode_step or mla_decode_absorbed_static, from any host thread) makes its MMA warp wait
+ * for a barrier phase that nothing completes. After limit_ns (1 .. 2e9) the wait gives up, the
+ * device status word latches MLA_ERR_TIMEOUT and every CTA stops early, after its TMA copies
+ * have landed and its MMAs have completed; that call's output is then undefined. The device
+ * stays usable and the next call runs normally. Returns MLA_ERR_INVALID_ARG for limits outside
+ * the range. */
+mla_status_t mla_debug_arm_wait_timeout(int64_t limit_ns);
+
 /* Static description of a status code. */
 const char* mla_status_string(mla_status_t status);
 

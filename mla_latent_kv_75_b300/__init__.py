@@ -80,6 +80,8 @@ for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
     _f.restype = ctypes.c_int32
+_lib.mla_debug_arm_wait_timeout.argtypes = [ctypes.c_int64]
+_lib.mla_debug_arm_wait_timeout.restype = ctypes.c_int32
 _lib.mla_status_string.argtypes = [ctypes.c_int32]
 _lib.mla_status_string.restype = ctypes.c_char_p
 _lib.mla_trace_arm.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int32),
@@ -229,6 +231,11 @@ def mla_prefill(dims, weights, h, cu_seqlens, B, n_tok, max_T, cache, ws, ws_byt
                             _ptr(cu_seqlens), int(B), int(n_tok), int(max_T),
                             ctypes.byref(cache), _ptr(ws), int(ws_bytes), _ptr(o),
                             _stream(stream)), "mla_prefill")
+
+
+def mla_debug_arm_wait_timeout(limit_ns: int) -> None:
+    """Make the next decode attention launch's bounded wait run out after limit_ns (test hook)."""
+    _check(_lib.mla_debug_arm_wait_timeout(int(limit_ns)), "mla_debug_arm_wait_timeout")
 
 
 def mla_get_device_status(stream=None) -> int:

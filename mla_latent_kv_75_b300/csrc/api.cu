@@ -327,6 +327,12 @@ mla_status_t mla_get_device_status(void* stream) {
   return (mla_status_t)v;
 }
 
+mla_status_t mla_debug_arm_wait_timeout(int64_t limit_ns) {
+  if (limit_ns <= 0 || limit_ns > 2000000000ll) return MLA_ERR_INVALID_ARG;
+  arm_decode_wait_timeout(limit_ns);
+  return MLA_OK;
+}
+
 const char* mla_status_string(mla_status_t s) {
   switch (s) {
     case MLA_OK: return "ok";

@@ -32,6 +32,7 @@
 // the merge.
 #include <stdlib.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -73,7 +74,7 @@ constexpr float kTau = 8.f;  // lazy rescale threshold (log2 units): p <= 2^8 be
 
 struct Shared {
   uint64_t full[kStages], empty_a[kStages], empty_b[kStages];
-  uint64_t s_full, s_free, p_full, pv_done, q_full, mma_done;
+  uint64_t s_full, s_free, p_full, pv_done, q_full, mma_done, never;
   uint32_t tmem_slot;
   int abort;
   int b0, j0, nt, nospan;
@@ -197,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const int32_t* __restrict__ seq_len,
                           const int64_t* __restrict__ seq_base, int64_t capacity, int B,
                           int max_len, float scale_log2, float* __restrict__ part_o,
-                          float* __restrict__ part_ml, int2* __restrict__ seq_slots) {
+                          float* __restrict__ part_ml, int2* __restrict__ seq_slots,
+                          int64_t test_stall_ns) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -224,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.q_full, 4);
     mbar_init(&sh.mma_done, 1);
+    mbar_init(&sh.never, 1);  // completed by nobody (the wait-timeout test)
     sh.abort = 0;
     sh.b0 = 0;
     sh.j0 = 0;
@@ -361,7 +364,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    bool ok = warp_wait(&sh.q_full, 0, abort);
+    bool ok = true;
+    if (test_stall_ns > 0) {
+      // Test of the bounded waits: wait for a barrier phase that nothing completes, give up
+      // after test_stall_ns, latch MLA_ERR_TIMEOUT and make the CTA's other roles give up too
+      // (they drain their own copies and exit).
+      const uint64_t t0 = global_ns();
+      for (;;) {  // lane 0 polls and decides for the warp
+        int state = 0;  // 1: the phase completed, 2: gave up
+        if (lane == 0)
+          state = mbar_try_wait(&sh.never, 0) ? 1
+                                              : (global_ns() - t0 > (uint64_t)test_stall_ns ? 2 : 0);
+        state = __shfl_sync(0xffffffffu, state, 0);
+        if (state == 1) break;
+        if (state == 2) {
+          if (lane == 0) {
+            flag_status(MLA_ERR_TIMEOUT);
+            *abort = 1;
+          }
+          ok = false;
+          break;
+        }
+      }
+    }
+    ok = ok && warp_wait(&sh.q_full, 0, abort);
     if (ok) {
       tc_fence_after();
       ok = issue_s(0);
@@ -841,6 +867,9 @@ Layout layout(int B) {
 }
 
 constexpr int kMaxDevices = 64;
+
+// One-shot wait-timeout test (mla_debug_arm_wait_timeout): consumed by the next launch.
+std::atomic<int64_t> g_test_stall_ns{0};
 std::mutex g_mu;
 int g_pairs[kMaxDevices] = {};
 
@@ -892,6 +921,7 @@ mla_status_t unabsorb_setup() {
 }  // namespace
 
 size_t tc_decode_ws(const mla_dims_t*, int B) { return layout(B).total; }
+void arm_decode_wait_timeout(int64_t limit_ns) { g_test_stall_ns.store(limit_ns); }
 size_t tc_decode_qt_offset(int B) { return layout(B).off_qt; }
 
 mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* q_c,
@@ -946,7 +976,8 @@ mla_status_t tc_decode_latent(const mla_dims_t* d, const mla_weights_t* w, const
     TraceScope ts(K_DECODE_ATTN, st);
     decode_attn_tc_kernel<<<2 * pairs, kThreads, kSmemBytes, st>>>(
         tm_rows, tm_qt, tm_qr, qt, seq_len, cache->seq_base,
-        cache->capacity, B, max_len, scale_log2, part, ml, rng);
+        cache->capacity, B, max_len, scale_log2, part, ml, rng,
+        g_test_stall_ns.exchange(0));
     s = launch_status();
     if (s != MLA_OK) return s;
   }

@@ -75,6 +75,7 @@ mla_status_t tc_prefill(const mla_dims_t* d, const mla_weights_t* w, const void*
 
 // Tensor-core absorbed decode (V2 widths, bf16): decode_tc.cu
 size_t tc_decode_ws(const mla_dims_t* d, int B);
+void arm_decode_wait_timeout(int64_t limit_ns);  // mla_debug_arm_wait_timeout
 size_t tc_decode_qt_offset(int B);  // byte offset of the q~ area in the decode workspace
 mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* q_c,
                        const void* q_r, const mla_cache_t* cache, const int32_t* seq_len, int B,

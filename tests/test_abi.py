@@ -98,3 +98,8 @@ def test_zero_sized_calls_are_no_ops():
                           0, ctypes.byref(cache), None) == 0
     assert mla.raw_status("mla_decode_absorbed", ctypes.byref(d), ctypes.byref(w), None, None,
                           ctypes.byref(cache), None, 0, 0, None, 0, None, None) == 0
+
+
+def test_wait_timeout_hook_checks_its_limit_on_the_host():
+    assert mla.raw_status("mla_debug_arm_wait_timeout", ctypes.c_int64(0)) == 1
+    assert mla.raw_status("mla_debug_arm_wait_timeout", ctypes.c_int64(3_000_000_000)) == 1
