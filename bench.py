@@ -545,6 +545,9 @@ def run_ours(args, rank, world, local_rank):
     prefill = None
     if not args.no_prefill:
         prefill = run_prefill(args, dev, peaks, flush)
+    out_proj = None
+    if not args.no_extra_configs:
+        out_proj = run_output_projection(args, dev, peaks, flush)
 
     if rank == 0:
         line = {
@@ -556,11 +559,54 @@ def run_ours(args, rank, world, local_rank):
             "decode_call": main["decode_call"], "decode_latent_call": main["decode_latent_call"],
             "step_roofline_frac": main["step_roofline_frac"], "kernels": main["kernels"],
             "three_call_step": main["three_call_step"], "configs": configs, "prefill": prefill,
+            "output_projection": out_proj,
             "cpu_baseline": main.get("cpu_baseline"), "e2e": main["e2e"],
             "gpu_launches": main["gpu_launches"], "clocks": clocks, "fast_path": main["fast_path"],
             "build": build_info(),
         }
         print(json.dumps(line), flush=True)
+
+
+def run_output_projection(args, dev, peaks, flush):
+    """u = W^O [o_1; ...; o_{n_h}] at the decode batch (16 tokens: W^O streaming, HBM-bound)
+    and at the prefill size (8192 tokens: tensor-bound), through mla_output_projection."""
+    import torch
+    import mla_latent_kv_75_b300 as mla
+    from mla_latent_kv_75_b300 import host
+    d = mi.V2
+    dims = host.dims_struct(d, "bf16")
+    W_O = host.to_device(mi.output_weight(d, "bf16"), "bf16", dev)
+    K = d.n_h * d.d_hc
+    out = {}
+    for n in (16, 8192):
+        o = torch.randn((n, K), device=dev, dtype=torch.float32)
+        u = torch.empty((n, d.d), device=dev, dtype=torch.float32)
+        ws_bytes = mla.mla_output_projection_workspace_size(dims, n)
+        ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+        call = lambda: mla.mla_output_projection(dims, W_O, o, n, ws, ws_bytes, u)
+        for _ in range(3):
+            flush()
+            call()
+        assert mla.mla_get_device_status() == 0
+        steps = max(1, min(args.steps, 10))
+        ms, launches = time_steps(call, steps, flush, trace_capacity=4 * steps, hold_ms=0.5)
+        per = {}
+        for name, t in launches:
+            per.setdefault(name, []).append(t)
+        t_s = statistics.mean(ms) * 1e-3
+        alg_bytes = d.d * K * 2 + n * K * 4 + n * d.d * 4
+        flops = 2 * n * K * d.d
+        floor_s = max(alg_bytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+        out["n%d" % n] = {"us": round(t_s * 1e6, 2), "alg_bytes": alg_bytes, "alg_flops": flops,
+                          "GB_s": round(alg_bytes / t_s / 1e9, 1),
+                          "TFLOP_s": round(flops / t_s / 1e12, 2),
+                          "roofline_frac": round(floor_s / t_s, 4),
+                          "kernels_us": {k: round(statistics.mean(v) * 1e3, 2)
+                                         for k, v in per.items()}}
+        del o, u, ws
+    del W_O
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_prefill(args, dev, peaks, flush):

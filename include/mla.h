@@ -176,6 +176,18 @@ mla_status_t mla_decode_step(const mla_dims_t* dims, const mla_weights_t* w, con
                              int32_t B, int32_t max_len, void* ws, size_t ws_bytes, float* o,
                              void* stream);
 
+/* Workspace needed by mla_output_projection for n tokens (0 on the SIMT path). */
+mla_status_t mla_output_projection_workspace_size(const mla_dims_t* dims, int32_t n,
+                                                  size_t* bytes);
+
+/* Output projection ([notes] §三分支计算 ④): u_t = W^O [o_{t,1}; ...; o_{t,n_h}], the per-head
+ * outputs of token t concatenated head by head. o [n, n_h, d_h^C] float32 (as mla_decode_* and
+ * mla_prefill write it); W_O [d, n_h*d_h^C] row-major in dtype (applied as y = W x); output
+ * u [n, d] float32. Accumulation in fp32; on the tensor-core path o enters the MMA as a hi/lo
+ * pair of bf16 (o = hi + lo to about 2^-16) held in ws. */
+mla_status_t mla_output_projection(const mla_dims_t* dims, const void* W_O, const float* o,
+                                   int32_t n, void* ws, size_t ws_bytes, float* u, void* stream);
+
 /* Scratch capacity of mla_decode_absorbed_static, in bytes (32 MiB). */
 #define MLA_STATIC_WS_BYTES (32u << 20)
 

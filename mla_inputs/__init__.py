@@ -29,7 +29,7 @@ import numpy as np
 # Stream ids: one per tensor kind (fixed forever so that stored expectations stay valid).
 _STREAM = {
     "W_DQ": 1, "W_UQ": 2, "W_QR": 3, "W_DKV": 4, "W_KR": 5, "W_UK": 6, "W_UV": 7,
-    "lengths": 8, "h": 9, "aux": 10,
+    "lengths": 8, "h": 9, "aux": 10, "W_O": 11,
 }
 
 WEIGHT_NAMES = ("W_DQ", "W_UQ", "W_QR", "W_DKV", "W_KR", "W_UK", "W_UV")
@@ -174,6 +174,15 @@ def weights(dims: Dims, dtype: str, seed: int = 0) -> Dict[str, np.ndarray]:
         w = rng.standard_normal((o, i), dtype=np.float32) * np.float32(1.0 / np.sqrt(i))
         out[name] = _finish(w, dtype)
     return out
+
+
+def output_weight(dims: Dims, dtype: str, seed: int = 0) -> np.ndarray:
+    """The output projection W^O [d, n_h * d_h^C], W ~ N(0, 1/(n_h d_h^C)); drawn apart from
+    the seven MLA matrices (it is 168 MB at the V2 widths)."""
+    fan_in = dims.n_h * dims.d_hc
+    rng = np.random.default_rng([seed, _STREAM["W_O"]])
+    w = rng.standard_normal((dims.d, fan_in), dtype=np.float32) * np.float32(1.0 / np.sqrt(fan_in))
+    return _finish(w, dtype)
 
 
 def hidden(dims: Dims, dtype: str, seq: int, n: int, seed: int = 0, start: int = 0) -> np.ndarray:

@@ -72,6 +72,8 @@ _SIGS = {
     "mla_decode_absorbed_latent": [_PD, _PW, _P, _P, _PC, _P, _I, _I, _P, ctypes.c_size_t, _P,
                                    _P],
     "mla_decode_step_workspace_size": [_PD, _I, _I, _SZ],
+    "mla_output_projection_workspace_size": [_PD, _I, _SZ],
+    "mla_output_projection": [_PD, _P, _P, _I, _P, ctypes.c_size_t, _P, _P],
     "mla_decode_step": [_PD, _PW, _P, _P, _PC, _P, _I, _I, _P, ctypes.c_size_t, _P, _P],
     "mla_get_device_status": [_P],
     "mla_fast_path": [_PD],
@@ -203,6 +205,20 @@ def mla_decode_step(dims, weights, h, pos, cache, seq_len, B, max_len, ws, ws_by
                                 ctypes.byref(cache), _ptr(seq_len), int(B), int(max_len),
                                 _ptr(ws), int(ws_bytes), _ptr(o), _stream(stream)),
            "mla_decode_step")
+
+
+def mla_output_projection_workspace_size(dims, n) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.mla_output_projection_workspace_size(ctypes.byref(dims), int(n),
+                                                     ctypes.byref(out)),
+           "mla_output_projection_workspace_size")
+    return out.value
+
+
+def mla_output_projection(dims, W_O, o, n, ws, ws_bytes, u, stream=None) -> None:
+    _check(_lib.mla_output_projection(ctypes.byref(dims), _ptr(W_O), _ptr(o), int(n), _ptr(ws),
+                                      int(ws_bytes), _ptr(u), _stream(stream)),
+           "mla_output_projection")
 
 
 MLA_STATIC_WS_BYTES = 32 << 20

@@ -63,7 +63,7 @@ TraceState g_trace;
 const char* const kKernelNames[K_NUM_IDS] = {
     "append", "q_down", "q_up", "absorb", "decode_attn", "decode_combine", "token_map",
     "prefill_append", "prefill_q_down", "prefill_q_up", "expand_k", "expand_v", "prefill_attn",
-    "decode_merge", "unabsorb", "q_absorb", "down"};
+    "decode_merge", "unabsorb", "q_absorb", "down", "out_split", "out_proj"};
 }  // namespace
 
 void trace_before(int kernel_id, cudaStream_t st) {
@@ -325,6 +325,30 @@ mla_status_t mla_get_device_status(void* stream) {
     if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return MLA_ERR_CUDA;
   }
   return (mla_status_t)v;
+}
+
+mla_status_t mla_output_projection_workspace_size(const mla_dims_t* d, int32_t n, size_t* bytes) {
+  MLA_TRY(check_dims(d));
+  if (!bytes || n < 0) return MLA_ERR_INVALID_ARG;
+  *bytes = fast_dims(d) ? tc_output_projection_ws(d, n) : 0;
+  return MLA_OK;
+}
+
+mla_status_t mla_output_projection(const mla_dims_t* d, const void* W_O, const float* o,
+                                   int32_t n, void* ws, size_t ws_bytes, float* u,
+                                   void* stream) {
+  MLA_TRY(check_dims(d));
+  if (n < 0) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  MLA_TRY(check_ptr(W_O));
+  MLA_TRY(check_ptr(o));
+  MLA_TRY(check_ptr(u));
+  size_t need = 0;
+  MLA_TRY(mla_output_projection_workspace_size(d, n, &need));
+  if (need && (!ws || ws_bytes < need)) return MLA_ERR_WORKSPACE;
+  if (need) MLA_TRY(check_ptr(ws));
+  if (fast_dims(d)) return tc_output_projection(d, W_O, o, n, ws, u, as_stream(stream));
+  return simt_output_projection(d, W_O, o, n, u, as_stream(stream));
 }
 
 mla_status_t mla_debug_arm_wait_timeout(int64_t limit_ns) {

@@ -5,6 +5,7 @@
 // output tile: warp 0 streams 64-wide K slices of W and X into a shared-memory ring with TMA,
 // warp 1 issues tcgen05.mma, warps 2..5 read the accumulator from TMEM and run the epilogue
 // (RoPE on pairs of adjacent output rows, cache-row scatter, dtype conversion).
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <set>
@@ -513,6 +514,38 @@ struct EpStoreBF16 {
   }
 };
 
+// Plain store Y[n * ld + o] in fp32.
+struct EpStoreF32 {
+  float* y;
+  int64_t ld;
+  __device__ void operator()(int o, int n, float v, float) const { y[(int64_t)n * ld + o] = v; }
+  __device__ void row32(int o, int nb, int N, const float* v, const float*) const {
+    float* p = y + (int64_t)nb * ld + o;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (nb + j >= N) break;
+      p[(int64_t)j * ld] = v[j];
+    }
+  }
+};
+
+// x (float32) -> hi + lo, two bf16 arrays with x = hi + lo to about 2^-16 relative; count is a
+// multiple of 4 and the pointers are 16-byte aligned.
+__global__ void __launch_bounds__(256) split_hi_lo_kernel(const float4* __restrict__ x,
+                                                          uint2* __restrict__ hi,
+                                                          uint2* __restrict__ lo, int64_t n4) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 v = x[i];
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+    const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - __low2float(h01), v.y - __high2float(h01));
+    const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - __low2float(h23), v.w - __high2float(h23));
+    hi[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+    lo[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
+  }
+}
+
 // Plain store Y[n * ld + o] in fp16.
 struct EpStoreF16 {
   __half* y;
@@ -967,6 +1000,39 @@ mla_status_t tc_expand(const void* W, int O, const void* latent, int64_t ld_late
     return launch_proj(a, ep, st);
   }
   EpStoreBF16 ep{(__nv_bfloat16*)y, nullptr, O};
+  return launch_proj(a, ep, st);
+}
+
+// Output projection ("MLA前向计算流程" §三分支计算 ④): u[n, :] = W^O o[n, :] with o [n, n_h*d_hc]
+// float32, applied as one GEMM of K = n_h*d_hc over o's hi/lo bf16 split (o = hi + lo to
+// ~2^-16, one MMA of width 2*BN covers both); ws holds the split.
+size_t tc_output_projection_ws(const mla_dims_t* d, int n) {
+  return 2 * align_up((size_t)n * d->n_h * d->d_hc * 2, 256);
+}
+
+mla_status_t tc_output_projection(const mla_dims_t* d, const void* W_O, const float* o, int n,
+                                  void* ws, float* u, cudaStream_t st) {
+  const int K = d->n_h * d->d_hc;
+  char* hi = (char*)ws;
+  char* lo = hi + align_up((size_t)n * K * 2, 256);
+  const int64_t n4 = (int64_t)n * K / 4;
+  {
+    TraceScope ts(K_OUT_SPLIT, st);
+    split_hi_lo_kernel<<<(int)std::min<int64_t>((n4 + 255) / 256, 4 * 148), 256, 0, st>>>(
+        (const float4*)o, (uint2*)hi, (uint2*)lo, n4);
+    mla_status_t s = launch_status();
+    if (s != MLA_OK) return s;
+  }
+  ProjArgs a{};
+  a.W0 = W_O;
+  a.O0 = d->d;
+  a.K = K;
+  a.X = hi;
+  a.X2 = lo;
+  a.ldx = K;
+  a.N = n;
+  a.kid = K_OUT_PROJ;
+  EpStoreF32 ep{u, d->d};
   return launch_proj(a, ep, st);
 }
 

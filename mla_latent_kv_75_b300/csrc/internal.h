@@ -11,7 +11,7 @@ namespace mla {
 enum KernelId : int {
   K_APPEND = 0, K_Q_DOWN, K_Q_UP, K_ABSORB, K_DECODE_ATTN, K_DECODE_COMBINE, K_TOKEN_MAP,
   K_PREFILL_APPEND, K_PREFILL_Q_DOWN, K_PREFILL_Q_UP, K_EXPAND_K, K_EXPAND_V, K_PREFILL_ATTN,
-  K_DECODE_MERGE, K_UNABSORB, K_Q_ABSORB, K_DOWN, K_NUM_IDS
+  K_DECODE_MERGE, K_UNABSORB, K_Q_ABSORB, K_DOWN, K_OUT_SPLIT, K_OUT_PROJ, K_NUM_IDS
 };
 
 // Launch tracing (host side): while armed, trace_before/trace_after record caller-owned
@@ -45,7 +45,13 @@ mla_status_t simt_prefill(const mla_dims_t* d, const mla_weights_t* w, const voi
                           const int32_t* cu, int B, int n, int max_T, mla_cache_t* cache,
                           void* ws, float* o, cudaStream_t st);
 
+mla_status_t simt_output_projection(const mla_dims_t* d, const void* W_O, const float* o, int n,
+                                    float* u, cudaStream_t st);
+
 // Tensor-core kernels (V2 widths, bf16): gemm_tc.cu
+size_t tc_output_projection_ws(const mla_dims_t* d, int n);
+mla_status_t tc_output_projection(const mla_dims_t* d, const void* W_O, const float* o, int n,
+                                  void* ws, float* u, cudaStream_t st);
 bool fast_dims(const mla_dims_t* d);
 mla_status_t tc_append(const mla_dims_t* d, const mla_weights_t* w, const void* h,
                        const int32_t* seq_idx, const int32_t* pos, int n, mla_cache_t* cache,

@@ -688,4 +688,22 @@ mla_status_t simt_prefill(const mla_dims_t* d, const mla_weights_t* w, const voi
   return prefill_t<float>(d, w, h, cu, B, n, max_T, cache, ws, o, st);
 }
 
+// ==================================================================================
+// Output projection (§三分支计算 ④): u[n, :] = W^O [o_{n,1}; ...; o_{n,n_h}], with o given as
+// [n, n_h * d_hc] float32 (the head-major concatenation is the row layout of o).
+// ==================================================================================
+mla_status_t simt_output_projection(const mla_dims_t* d, const void* W_O, const float* o, int n,
+                                    float* u, cudaStream_t st) {
+  const int K = d->n_h * d->d_hc;
+  if (d->dtype == MLA_BF16)
+    launch_linear<float, __nv_bfloat16>(K_OUT_PROJ, o, K, nullptr, n,
+                                        (const __nv_bfloat16*)W_O, d->d,
+                                        (const __nv_bfloat16*)W_O, d->d, K,
+                                        StoreF32Ep{u, d->d}, st);
+  else
+    launch_linear<float, float>(K_OUT_PROJ, o, K, nullptr, n, (const float*)W_O, d->d,
+                                (const float*)W_O, d->d, K, StoreF32Ep{u, d->d}, st);
+  return launch_status();
+}
+
 }  // namespace mla

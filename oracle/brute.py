@@ -90,3 +90,17 @@ def prefill(h_rows: List[Sequence[float]], W: Dict[str, list], dims: dict):
 def to_lists(W: dict) -> Dict[str, list]:
     """Convert array-like weights to nested Python lists of floats."""
     return {k: [[float(x) for x in row] for row in v] for k, v in W.items()}
+
+
+def output_projection(o_heads: List[List[float]], W_O: List[List[float]]) -> List[float]:
+    """u = W^O [o_1; ...; o_{n_h}] for one token, with scalar loops: element k of head i is
+    input column i * d_hc + k of W^O."""
+    d_hc = len(o_heads[0])
+    u = []
+    for row in W_O:
+        acc = 0.0
+        for i, oi in enumerate(o_heads):
+            for k in range(d_hc):
+                acc += row[i * d_hc + k] * oi[k]
+        u.append(acc)
+    return u

@@ -197,6 +197,16 @@ def decode_explicit(q_c, q_r, rows: List[np.ndarray], W_UK, W_UV, d_c: int,
     return out
 
 
+def output_projection(o, W_O) -> np.ndarray:
+    """④ output: u_t = W^O [o_{t,1}; ...; o_{t,n_h}], the per-head outputs of token t
+    concatenated head by head and mapped back to the hidden width.
+
+    o [..., n_h, d_hc], W_O [d, n_h * d_hc] -> u [..., d].
+    """
+    o = _f64(o)
+    return o.reshape(o.shape[:-2] + (o.shape[-2] * o.shape[-1],)) @ _f64(W_O).T
+
+
 def absorb_query(q_c, W_UK, n_h: int, d_hc: int) -> np.ndarray:
     """q~_i = (W^UK_i)^T q^C_i, the latent-space query ("从LLaMA到DeepSeek" §六).
 

@@ -185,6 +185,24 @@ def test_vectorised_prefill_matches_scalar_brute_force(dims, T):
     np.testing.assert_allclose(o, np.array(ob), rtol=1e-11, atol=1e-12)
 
 
+@pytest.mark.parametrize("dims", [MICRO, mi.TINY])
+def test_output_projection_matches_scalar_brute_force(dims):
+    """u = W^O [o_1; ...; o_{n_h}]: the head-major concatenation against scalar loops, on
+    shapes where every width differs (a head/feature transposition cannot go unnoticed)."""
+    W_O = mi.output_weight(dims, "f32")
+    assert W_O.shape == (dims.d, dims.n_h * dims.d_hc)
+    o = mi.aux_normal((3, dims.n_h, dims.d_hc), index=40)
+    u = ref.output_projection(o, W_O)
+    Wl = [[float(x) for x in row] for row in W_O]
+    for t in range(3):
+        ub = brute.output_projection([[float(x) for x in oi] for oi in o[t]], Wl)
+        np.testing.assert_allclose(u[t], ub, rtol=1e-12, atol=1e-12)
+    # one head's output reaches u only through its own block of W^O
+    one = np.zeros((dims.n_h, dims.d_hc))
+    one[1, 2] = 1.0
+    np.testing.assert_allclose(ref.output_projection(one, W_O), W_O[:, dims.d_hc + 2], atol=0)
+
+
 def test_tiny_decode_matches_scalar_brute_force():
     """The fp32 tiny workload end to end (64 cached tokens + one new token at position 64)."""
     wl = mi.workload("tiny_f32")
