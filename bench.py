@@ -545,9 +545,10 @@ def run_ours(args, rank, world, local_rank):
     prefill = None
     if not args.no_prefill:
         prefill = run_prefill(args, dev, peaks, flush)
-    out_proj = None
+    out_proj = query_variants = None
     if not args.no_extra_configs:
         out_proj = run_output_projection(args, dev, peaks, flush)
+        query_variants = run_query_variants(args, dev, peaks, flush)
 
     if rank == 0:
         line = {
@@ -559,7 +560,7 @@ def run_ours(args, rank, world, local_rank):
             "decode_call": main["decode_call"], "decode_latent_call": main["decode_latent_call"],
             "step_roofline_frac": main["step_roofline_frac"], "kernels": main["kernels"],
             "three_call_step": main["three_call_step"], "configs": configs, "prefill": prefill,
-            "output_projection": out_proj,
+            "output_projection": out_proj, "query_variants": query_variants,
             "cpu_baseline": main.get("cpu_baseline"), "e2e": main["e2e"],
             "gpu_launches": main["gpu_launches"], "clocks": clocks, "fast_path": main["fast_path"],
             "build": build_info(),
@@ -605,6 +606,55 @@ def run_output_projection(args, dev, peaks, flush):
                                          for k, v in per.items()}}
         del o, u, ws
     del W_O
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_query_variants(args, dev, peaks, flush):
+    """The absorbed decode query two ways, at 16 and 128 tokens: the fused two-product kernel
+    (mla_project_q_absorbed: W^UQ, W^QR and W^UK streamed, 92 MB) against the pre-merged map
+    (mla_project_q_premerged: W^UQK = (W^UK_i)^T W^UQ_i formed once, 201 MB, with W^QR); both
+    include the c^Q down-projection. Per-call device time and the call's HBM roofline."""
+    import torch
+    import mla_latent_kv_75_b300 as mla
+    from mla_latent_kv_75_b300 import host
+    d = mi.V2
+    model = host.DeviceModel.upload(d, "bf16", mi.weights(d, "bf16"), dev)
+    dims, w = model.abi_dims, model.abi_weights
+    W_UQK = torch.empty((d.n_h * d.d_c, d.d_cq), dtype=torch.bfloat16, device=dev)
+    mla.mla_merge_query_absorption(dims, model.W["W_UQ"], model.W["W_UK"], W_UQK)
+    assert mla.mla_get_device_status() == 0
+    wbytes = {"fused": (d.d_cq * d.d + d.n_h * (d.d_hc + d.d_hr) * d.d_cq + d.n_h * d.d_hc * d.d_c) * 2,
+              "premerged": (d.d_cq * d.d + d.n_h * (d.d_c + d.d_hr) * d.d_cq) * 2}
+    out = {"weight_bytes": wbytes}
+    for n in (16, 128):
+        h = torch.randn((n, d.d), device=dev).to(torch.bfloat16)
+        pos = torch.arange(n, dtype=torch.int32, device=dev) * 37
+        ws_bytes = mla.mla_project_q_workspace_size(dims, n)
+        ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+        q_t = torch.empty((n, d.n_h, d.d_c), dtype=torch.bfloat16, device=dev)
+        q_r = torch.empty((n, d.n_h, d.d_hr), dtype=torch.bfloat16, device=dev)
+        calls = {"fused": lambda: mla.mla_project_q_absorbed(dims, w, h, pos, n, ws, ws_bytes, q_t, q_r),
+                 "premerged": lambda: mla.mla_project_q_premerged(dims, w, W_UQK, h, pos, n, ws,
+                                                                  ws_bytes, q_t, q_r)}
+        res = {}
+        for name, call in calls.items():
+            for _ in range(3):
+                flush()
+                call()
+            assert mla.mla_get_device_status() == 0
+            steps = max(1, min(args.steps, 10))
+            _, launches = time_steps(call, steps, flush, trace_capacity=4 * steps, hold_ms=0.5)
+            per = {}
+            for k, t in launches:
+                per.setdefault(k, []).append(t)
+            us = sum(statistics.mean(v) for v in per.values()) * 1e3
+            alg = wbytes[name] + n * d.d * 2 + n * d.n_h * (d.d_c + d.d_hr) * 2
+            res[name] = {"us": round(us, 2), "alg_bytes": alg,
+                         "roofline_frac": round(alg / (peaks["hbm_gbs"] * 1e9) / (us * 1e-6), 4),
+                         "kernels_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in per.items()}}
+        out["n%d" % n] = res
+    del model, W_UQK
     torch.cuda.empty_cache()
     return out
 

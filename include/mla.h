@@ -176,6 +176,27 @@ mla_status_t mla_decode_step(const mla_dims_t* dims, const mla_weights_t* w, con
                              int32_t B, int32_t max_len, void* ws, size_t ws_bytes, float* o,
                              void* stream);
 
+/* Pre-merged absorbed query weights ([llama] §六: W^UQ and W^UK are both fixed, so the
+ * product can be formed once, offline): for every head i,
+ *   W^UQK_i = (W^UK_i)^T W^UQ_i   [d_c x d_c'],
+ * written as W_UQK [n_h*d_c, d_c'] row-major in dtype (head i's block is rows i*d_c ..
+ * (i+1)*d_c-1). fp32 accumulation, one rounding to dtype. A one-off: a plain SIMT kernel. At the
+ * V2 widths W_UQK is 128*512*1536 values (201 MB in bf16), against 50 MB of W^UQ plus 17 MB of
+ * W^UK for the fused two-product path (mla_project_q_absorbed). */
+mla_status_t mla_merge_query_absorption(const mla_dims_t* dims, const void* W_UQ,
+                                        const void* W_UK, void* W_UQK, void* stream);
+
+/* Query projection with pre-merged weights: c^Q = W^DQ h, q~_{t,i} = W^UQK_i c^Q (one product
+ * per head, d_c wide), q^R_{t,i} = RoPE(W^QR_i c^Q). Same inputs, outputs and workspace as
+ * mla_project_q_absorbed (q_t [n, n_h, d_c], q_r [n, n_h, d_h^R] in dtype; workspace
+ * mla_project_q_workspace_size(n)), with W_UQK from mla_merge_query_absorption in place of
+ * W_UQ and W_UK. Uses W_DQ and W_QR from w. Any dims (tensor-core path for the V2 widths in
+ * bf16, SIMT otherwise). */
+mla_status_t mla_project_q_premerged(const mla_dims_t* dims, const mla_weights_t* w,
+                                     const void* W_UQK, const void* h, const int32_t* pos,
+                                     int32_t n, void* ws, size_t ws_bytes, void* q_t, void* q_r,
+                                     void* stream);
+
 /* Workspace needed by mla_output_projection for n tokens (0 on the SIMT path). */
 mla_status_t mla_output_projection_workspace_size(const mla_dims_t* dims, int32_t n,
                                                   size_t* bytes);

@@ -73,6 +73,8 @@ _SIGS = {
                                    _P],
     "mla_decode_step_workspace_size": [_PD, _I, _I, _SZ],
     "mla_output_projection_workspace_size": [_PD, _I, _SZ],
+    "mla_merge_query_absorption": [_PD, _P, _P, _P, _P],
+    "mla_project_q_premerged": [_PD, _PW, _P, _P, _P, _I, _P, ctypes.c_size_t, _P, _P, _P],
     "mla_output_projection": [_PD, _P, _P, _I, _P, ctypes.c_size_t, _P, _P],
     "mla_decode_step": [_PD, _PW, _P, _P, _PC, _P, _I, _I, _P, ctypes.c_size_t, _P, _P],
     "mla_get_device_status": [_P],
@@ -205,6 +207,20 @@ def mla_decode_step(dims, weights, h, pos, cache, seq_len, B, max_len, ws, ws_by
                                 ctypes.byref(cache), _ptr(seq_len), int(B), int(max_len),
                                 _ptr(ws), int(ws_bytes), _ptr(o), _stream(stream)),
            "mla_decode_step")
+
+
+def mla_merge_query_absorption(dims, W_UQ, W_UK, W_UQK, stream=None) -> None:
+    _check(_lib.mla_merge_query_absorption(ctypes.byref(dims), _ptr(W_UQ), _ptr(W_UK),
+                                           _ptr(W_UQK), _stream(stream)),
+           "mla_merge_query_absorption")
+
+
+def mla_project_q_premerged(dims, weights, W_UQK, h, pos, n, ws, ws_bytes, q_t, q_r,
+                            stream=None) -> None:
+    _check(_lib.mla_project_q_premerged(ctypes.byref(dims), ctypes.byref(weights), _ptr(W_UQK),
+                                        _ptr(h), _ptr(pos), int(n), _ptr(ws), int(ws_bytes),
+                                        _ptr(q_t), _ptr(q_r), _stream(stream)),
+           "mla_project_q_premerged")
 
 
 def mla_output_projection_workspace_size(dims, n) -> int:

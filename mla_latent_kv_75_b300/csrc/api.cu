@@ -63,7 +63,8 @@ TraceState g_trace;
 const char* const kKernelNames[K_NUM_IDS] = {
     "append", "q_down", "q_up", "absorb", "decode_attn", "decode_combine", "token_map",
     "prefill_append", "prefill_q_down", "prefill_q_up", "expand_k", "expand_v", "prefill_attn",
-    "decode_merge", "unabsorb", "q_absorb", "down", "out_split", "out_proj"};
+    "decode_merge", "unabsorb", "q_absorb", "down", "out_split", "out_proj", "merge_w",
+    "q_premerged"};
 }  // namespace
 
 void trace_before(int kernel_id, cudaStream_t st) {
@@ -325,6 +326,50 @@ mla_status_t mla_get_device_status(void* stream) {
     if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return MLA_ERR_CUDA;
   }
   return (mla_status_t)v;
+}
+
+mla_status_t mla_merge_query_absorption(const mla_dims_t* d, const void* W_UQ, const void* W_UK,
+                                        void* W_UQK, void* stream) {
+  MLA_TRY(check_dims(d));
+  MLA_TRY(check_ptr(W_UQ));
+  MLA_TRY(check_ptr(W_UK));
+  MLA_TRY(check_ptr(W_UQK));
+  return simt_merge_absorption(d, W_UQ, W_UK, W_UQK, as_stream(stream));
+}
+
+mla_status_t mla_project_q_premerged(const mla_dims_t* d, const mla_weights_t* w,
+                                     const void* W_UQK, const void* h, const int32_t* pos,
+                                     int32_t n, void* ws, size_t ws_bytes, void* q_t, void* q_r,
+                                     void* stream) {
+  MLA_TRY(check_dims(d));
+  if (!w || n < 0) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  if (!pos) return MLA_ERR_INVALID_ARG;
+  MLA_TRY(check_ptr(h));
+  MLA_TRY(check_ptr(w->W_DQ));
+  MLA_TRY(check_ptr(w->W_QR));
+  MLA_TRY(check_ptr(W_UQK));
+  MLA_TRY(check_ptr(q_t));
+  MLA_TRY(check_ptr(q_r));
+  size_t need = 0;
+  MLA_TRY(mla_project_q_workspace_size(d, n, &need));
+  if (need && (!ws || ws_bytes < need)) return MLA_ERR_WORKSPACE;
+  if (need) MLA_TRY(check_ptr(ws));
+  // the merged matrix gives each head d_c query columns instead of d_h^C: the query
+  // up-projection with that width and W^UQK in place of W^UQ
+  mla_dims_t dm = *d;
+  dm.d_hc = d->d_c;
+  mla_weights_t wm = *w;
+  wm.W_UQ = W_UQK;
+  cudaStream_t st = as_stream(stream);
+  if (fast_dims(d)) {
+    char* hi = (char*)ws;
+    char* lo = hi + align_up((size_t)n * d->d_cq * 2, 256);
+    MLA_TRY(tc_q_down(d, w, h, n, hi, lo, K_Q_DOWN, st));
+    return tc_q_up(&dm, &wm, hi, lo, pos, n, q_t, q_r, (int64_t)d->n_h * d->d_c, d->d_c,
+                   (int64_t)d->n_h * d->d_hr, d->d_hr, false, K_Q_PREMERGED, st);
+  }
+  return simt_project_q(&dm, &wm, h, pos, n, ws, q_t, q_r, st);
 }
 
 mla_status_t mla_output_projection_workspace_size(const mla_dims_t* d, int32_t n, size_t* bytes) {

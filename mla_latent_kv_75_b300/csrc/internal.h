@@ -11,7 +11,7 @@ namespace mla {
 enum KernelId : int {
   K_APPEND = 0, K_Q_DOWN, K_Q_UP, K_ABSORB, K_DECODE_ATTN, K_DECODE_COMBINE, K_TOKEN_MAP,
   K_PREFILL_APPEND, K_PREFILL_Q_DOWN, K_PREFILL_Q_UP, K_EXPAND_K, K_EXPAND_V, K_PREFILL_ATTN,
-  K_DECODE_MERGE, K_UNABSORB, K_Q_ABSORB, K_DOWN, K_OUT_SPLIT, K_OUT_PROJ, K_NUM_IDS
+  K_DECODE_MERGE, K_UNABSORB, K_Q_ABSORB, K_DOWN, K_OUT_SPLIT, K_OUT_PROJ, K_MERGE_W, K_Q_PREMERGED, K_NUM_IDS
 };
 
 // Launch tracing (host side): while armed, trace_before/trace_after record caller-owned
@@ -45,6 +45,8 @@ mla_status_t simt_prefill(const mla_dims_t* d, const mla_weights_t* w, const voi
                           const int32_t* cu, int B, int n, int max_T, mla_cache_t* cache,
                           void* ws, float* o, cudaStream_t st);
 
+mla_status_t simt_merge_absorption(const mla_dims_t* d, const void* W_UQ, const void* W_UK,
+                                   void* W_UQK, cudaStream_t st);
 mla_status_t simt_output_projection(const mla_dims_t* d, const void* W_O, const float* o, int n,
                                     float* u, cudaStream_t st);
 

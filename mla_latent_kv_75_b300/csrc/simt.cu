@@ -706,4 +706,72 @@ mla_status_t simt_output_projection(const mla_dims_t* d, const void* W_O, const 
   return launch_status();
 }
 
+// ==================================================================================
+// Pre-merged absorbed query weights ("从LLaMA到DeepSeek[01] - MLA（上）" §六: W^UQ and W^UK are
+// both fixed, so their product can be formed once): for every head i,
+//   W^UQK_i [d_c x d_c'] = (W^UK_i)^T W^UQ_i,
+//   out[(i d_c + l) d_c' + c] = sum_d W^UK[i d_hc + d][l] W^UQ[i d_hc + d][c],
+// fp32 accumulation, stored in the weights' dtype. A one-off, so a plain tiled kernel: a
+// 64 x 64 output tile per block, the shared K dimension d (d_hc) in chunks of 32.
+// ==================================================================================
+template <typename T>
+__global__ void __launch_bounds__(256) merge_absorption_kernel(const T* __restrict__ W_UQ,
+                                                               const T* __restrict__ W_UK,
+                                                               int d_hc, int d_c, int d_cq,
+                                                               T* __restrict__ out) {
+  __shared__ float As[32][64 + 1];  // [d][l]
+  __shared__ float Bs[32][64 + 1];  // [d][c]
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;  // 4 c-columns x 4 l-rows each
+  const int c0 = blockIdx.x * 64, l0 = blockIdx.y * 64, i = blockIdx.z;
+  float acc[4][4] = {};
+  for (int d0 = 0; d0 < d_hc; d0 += 32) {
+    for (int e = tid; e < 32 * 64; e += 256) {
+      const int dd = e >> 6, x = e & 63, dr = d0 + dd;
+      const int64_t row = (int64_t)i * d_hc + dr;
+      As[dd][x] = (dr < d_hc && l0 + x < d_c) ? to_f(W_UK[row * d_c + l0 + x]) : 0.f;
+      Bs[dd][x] = (dr < d_hc && c0 + x < d_cq) ? to_f(W_UQ[row * d_cq + c0 + x]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int dd = 0; dd < 32; ++dd) {
+      float a[4], b[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        a[k] = As[dd][ty * 4 + k];
+        b[k] = Bs[dd][tx * 4 + k];
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int l = l0 + ty * 4 + r;
+    if (l >= d_c) continue;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int cc = c0 + tx * 4 + c;
+      if (cc < d_cq) out[((int64_t)i * d_c + l) * d_cq + cc] = from_f<T>(acc[r][c]);
+    }
+  }
+}
+
+mla_status_t simt_merge_absorption(const mla_dims_t* d, const void* W_UQ, const void* W_UK,
+                                   void* W_UQK, cudaStream_t st) {
+  const dim3 grid(ceil_div(d->d_cq, 64), ceil_div(d->d_c, 64), d->n_h);
+  TraceScope ts(K_MERGE_W, st);
+  if (d->dtype == MLA_BF16)
+    merge_absorption_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+        (const __nv_bfloat16*)W_UQ, (const __nv_bfloat16*)W_UK, d->d_hc, d->d_c, d->d_cq,
+        (__nv_bfloat16*)W_UQK);
+  else
+    merge_absorption_kernel<float><<<grid, 256, 0, st>>>((const float*)W_UQ, (const float*)W_UK,
+                                                         d->d_hc, d->d_c, d->d_cq,
+                                                         (float*)W_UQK);
+  return launch_status();
+}
+
 }  // namespace mla

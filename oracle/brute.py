@@ -104,3 +104,21 @@ def output_projection(o_heads: List[List[float]], W_O: List[List[float]]) -> Lis
                 acc += row[i * d_hc + k] * oi[k]
         u.append(acc)
     return u
+
+
+def merge_query_absorption(W_UQ: List[List[float]], W_UK: List[List[float]], n_h: int,
+                           d_hc: int) -> List[List[float]]:
+    """(W^UK_i)^T W^UQ_i for every head with scalar loops: row i*d_c + l, column c is
+    sum over d of W^UK[i*d_hc + d][l] * W^UQ[i*d_hc + d][c]."""
+    d_c, d_cq = len(W_UK[0]), len(W_UQ[0])
+    out = []
+    for i in range(n_h):
+        for l in range(d_c):
+            row = []
+            for c in range(d_cq):
+                acc = 0.0
+                for d in range(d_hc):
+                    acc += W_UK[i * d_hc + d][l] * W_UQ[i * d_hc + d][c]
+                row.append(acc)
+            out.append(row)
+    return out

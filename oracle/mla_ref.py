@@ -197,6 +197,17 @@ def decode_explicit(q_c, q_r, rows: List[np.ndarray], W_UK, W_UV, d_c: int,
     return out
 
 
+def merge_query_absorption(W_UQ, W_UK, n_h: int, d_hc: int) -> np.ndarray:
+    """The absorbed query map formed once ("从LLaMA到DeepSeek" §六: both factors are fixed):
+    W^UQK_i = (W^UK_i)^T W^UQ_i for every head, stacked head by head.
+
+    W_UQ [n_h*d_hc, d_cq], W_UK [n_h*d_hc, d_c] -> [n_h*d_c, d_cq].
+    """
+    uq = _f64(W_UQ).reshape(n_h, d_hc, -1)
+    uk = _f64(W_UK).reshape(n_h, d_hc, -1)
+    return np.einsum("hdl,hdc->hlc", uk, uq).reshape(-1, uq.shape[-1])
+
+
 def output_projection(o, W_O) -> np.ndarray:
     """④ output: u_t = W^O [o_{t,1}; ...; o_{t,n_h}], the per-head outputs of token t
     concatenated head by head and mapped back to the hidden width.

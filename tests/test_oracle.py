@@ -203,6 +203,25 @@ def test_output_projection_matches_scalar_brute_force(dims):
     np.testing.assert_allclose(ref.output_projection(one, W_O), W_O[:, dims.d_hc + 2], atol=0)
 
 
+def test_merged_absorption_matches_brute_force_and_associativity():
+    """W^UQK_i = (W^UK_i)^T W^UQ_i: scalar loops on a shape with distinct widths, and applying
+    the merged map to c^Q gives the absorbed query of the explicit two-step form."""
+    dims = MICRO
+    W = mi.weights(dims, "f32")
+    M = ref.merge_query_absorption(W["W_UQ"], W["W_UK"], dims.n_h, dims.d_hc)
+    assert M.shape == (dims.n_h * dims.d_c, dims.d_cq)
+    Mb = brute.merge_query_absorption(brute.to_lists({"a": W["W_UQ"]})["a"],
+                                      brute.to_lists({"a": W["W_UK"]})["a"], dims.n_h, dims.d_hc)
+    np.testing.assert_allclose(M, np.array(Mb), rtol=1e-12, atol=1e-12)
+    h = mi.hidden(dims, "f32", 0, 3).astype(np.float64)
+    c_q = h @ W["W_DQ"].T.astype(np.float64)
+    q_c, _ = ref.query(h, W["W_DQ"], W["W_UQ"], W["W_QR"], [0, 1, 2], dims.n_h, dims.d_hc,
+                       dims.d_hr, dims.rope_base)
+    q_t = ref.absorb_query(q_c, W["W_UK"], dims.n_h, dims.d_hc)
+    q_t_merged = (c_q @ M.T).reshape(3, dims.n_h, dims.d_c)
+    np.testing.assert_allclose(q_t_merged, q_t, rtol=1e-12, atol=1e-12)
+
+
 def test_tiny_decode_matches_scalar_brute_force():
     """The fp32 tiny workload end to end (64 cached tokens + one new token at position 64)."""
     wl = mi.workload("tiny_f32")
