@@ -122,3 +122,40 @@ def merge_query_absorption(W_UQ: List[List[float]], W_UK: List[List[float]], n_h
                 row.append(acc)
             out.append(row)
     return out
+
+
+def select_topk(scores: Sequence[float], k: int) -> List[int]:
+    """k rounds of 'take the largest remaining score, the lowest position among equals',
+    then the picked positions in increasing order."""
+    left = list(range(len(scores)))
+    picked = []
+    for _ in range(min(k, len(scores))):
+        best = left[0]
+        for j in left[1:]:
+            if scores[j] > scores[best]:
+                best = j
+        picked.append(best)
+        left.remove(best)
+    return sorted(picked)
+
+
+def sparse_attention_output(tok: List[dict], t: int, selected: Sequence[int], i: int,
+                            scale: float) -> List[float]:
+    """o_{t,i} over the selected key positions only: softmax over j in ``selected`` of
+    (q_{t,i} . k_{j,i}) * scale, weights applied to v_{j,i}."""
+    q = tok[t]["q_c"][i] + tok[t]["q_r"][i]
+    s = []
+    for j in selected:
+        k = tok[j]["k_c"][i] + tok[j]["k_r"]
+        acc = 0.0
+        for a, b in zip(q, k):
+            acc += a * b
+        s.append(acc * scale)
+    m = max(s)
+    e = [math.exp(x - m) for x in s]
+    z = sum(e)
+    o = [0.0] * len(tok[0]["v"][i])
+    for w_j, j in zip(e, selected):
+        for dd in range(len(o)):
+            o[dd] += (w_j / z) * tok[j]["v"][i][dd]
+    return o

@@ -307,3 +307,32 @@ def cache_counts(n_h: int, d_hc: int, d_hr: int, d_c: int, d_cq: int) -> Dict[st
         "ratio_c_kv": n_h * d_hc / d_c,
         "ratio_k_r": n_h * d_hr / d_hr,
     }
+
+
+# ---------------------------------------------------------------------------------
+# Top-k sparse selection before the decode ("MLA前向计算流程", version table, V3.2 + DSA
+# row: MLA itself is unchanged; an indexer picks top-k over the latent sequence and the core
+# attention still runs MLA over what was picked)
+# ---------------------------------------------------------------------------------
+
+def select_topk(scores, L: int, k: int) -> np.ndarray:
+    """Positions of the k largest index scores among positions 0..L-1, in increasing position
+    order. Equal scores rank the lower position first (-0.0 equals +0.0); L <= k selects every
+    position. The indexer that produces the scores is not defined by the pages: they are an
+    input here."""
+    s = np.asarray(scores, dtype=np.float64)[:L]
+    if L <= k:
+        return np.arange(L)
+    order = np.lexsort((np.arange(L), -s))  # primary key: score, descending; then position
+    return np.sort(order[:k])
+
+
+def decode_sparse(q_c, q_r, rows: List[np.ndarray], scores: List[np.ndarray], k: int, W_UK,
+                  W_UV, d_c: int, scale: Optional[float] = None,
+                  heads: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Decode of sequence b over its selected rows only: the same per-head attention as
+    ``decode_explicit`` with rows[b] replaced by rows[b][select_topk(scores[b], L_b, k)].
+    Every head attends to the same selected positions (the selection is over the shared
+    latent sequence)."""
+    picked = [_f64(r)[select_topk(sc, len(r), k)] for r, sc in zip(rows, scores)]
+    return decode_explicit(q_c, q_r, picked, W_UK, W_UV, d_c, scale=scale, heads=heads)

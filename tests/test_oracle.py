@@ -313,3 +313,86 @@ def test_round_bf16_agrees_with_the_generators_float32_rounding():
     x = mi.aux_normal((10000,), index=40, scale=3.0)
     np.testing.assert_array_equal(ref.round_bf16(x.astype(np.float64)),
                                   mi.round_to_bf16(x).astype(np.float64))
+
+
+# ------------------------------------------------------------------ top-k sparse selection
+
+def test_topk_selection_matches_scalar_brute_force():
+    """Scores from a small set (many ties, -0.0 beside +0.0) against k rounds of 'largest
+    remaining, lowest position first'."""
+    rng = np.random.default_rng(7)
+    values = np.array([-2.5, -1.0, -0.0, 0.0, 0.5, 3.0], dtype=np.float32)
+    for L in (1, 2, 5, 17, 40):
+        for k in (1, 2, 3, 8, 16, 64):
+            s = rng.choice(values, L)
+            want = brute.select_topk([float(x) for x in s], k)
+            got = ref.select_topk(s, L, k)
+            assert list(got) == want, (L, k)
+
+
+def test_topk_selection_special_cases():
+    L, k = 10, 4
+    assert list(ref.select_topk(np.zeros(L), L, k)) == [0, 1, 2, 3]  # all tied: lowest first
+    assert list(ref.select_topk(np.arange(L, dtype=float), L, k)) == [6, 7, 8, 9]
+    assert list(ref.select_topk(-np.arange(L, dtype=float), L, k)) == [0, 1, 2, 3]
+    assert list(ref.select_topk(np.arange(L, dtype=float), L, L + 3)) == list(range(L))
+    assert list(ref.select_topk(np.arange(L, dtype=float), 0, k)) == []
+    # only the first L scores count: larger scores past L are ignored
+    s = np.array([1.0, 2.0, 3.0, 100.0, 200.0])
+    assert list(ref.select_topk(s, 3, 2)) == [1, 2]
+    # -inf and huge values order like any other scores
+    s = np.array([-np.inf, 3e38, -3e38, np.inf, 0.0])
+    assert list(ref.select_topk(s, 5, 2)) == [1, 3]
+
+
+def _micro_tokens(T, seed=0):
+    dims = MICRO
+    W, h = _seq(dims, T, seq=seed)
+    pos = np.arange(T)
+    c, kr = ref.kv_latent(h, W["W_DKV"], W["W_KR"], pos, dims.rope_base)
+    rows = ref.cache_rows(c, kr)
+    q_c, q_r = ref.query(h[-1:], W["W_DQ"], W["W_UQ"], W["W_QR"], pos[-1:], dims.n_h,
+                         dims.d_hc, dims.d_hr, dims.rope_base)
+    return dims, W, h, rows, q_c, q_r
+
+
+def test_sparse_decode_matches_scalar_brute_force():
+    T, k = 9, 4
+    dims, W, h, rows, q_c, q_r = _micro_tokens(T)
+    scores = np.random.default_rng(3).standard_normal(T)
+    o = ref.decode_sparse(q_c, q_r, [rows], [scores], k, W["W_UK"], W["W_UV"], dims.d_c)
+    Wl = brute.to_lists(W)
+    dd = _dims_dict(dims)
+    tok = [brute.token_branches(list(map(float, h[p])), Wl, p, dd) for p in range(T)]
+    sel = brute.select_topk([float(x) for x in scores], k)
+    scale = 1.0 / math.sqrt(dims.d_hc + dims.d_hr)
+    for i in range(dims.n_h):
+        np.testing.assert_allclose(o[0, i], brute.sparse_attention_output(tok, T - 1, sel, i,
+                                                                          scale),
+                                   rtol=1e-11, atol=1e-12)
+
+
+def test_sparse_decode_with_k_at_least_the_length_is_the_dense_decode():
+    T = 7
+    dims, W, h, rows, q_c, q_r = _micro_tokens(T, seed=1)
+    scores = np.random.default_rng(4).standard_normal(T)
+    dense = ref.decode_explicit(q_c, q_r, [rows], W["W_UK"], W["W_UV"], dims.d_c)
+    for k in (T, T + 5):
+        sparse = ref.decode_sparse(q_c, q_r, [rows], [scores], k, W["W_UK"], W["W_UV"],
+                                   dims.d_c)
+        np.testing.assert_array_equal(sparse, dense)
+
+
+def test_sparse_decode_with_one_selected_row_returns_its_value():
+    """k = 1: the softmax over one key is 1, so o_i = W^UV_i c_{j*} for the top-scored j*."""
+    T = 8
+    dims, W, h, rows, q_c, q_r = _micro_tokens(T, seed=2)
+    scores = np.zeros(T)
+    scores[5] = 2.0
+    o = ref.decode_sparse(q_c, q_r, [rows], [scores], 1, W["W_UK"], W["W_UV"], dims.d_c)
+    c5 = rows[5, :dims.d_c]
+    for i in range(dims.n_h):
+        Wv = W["W_UV"][i * dims.d_hc:(i + 1) * dims.d_hc].astype(np.float64)
+        want = [sum(float(Wv[r, c]) * float(c5[c]) for c in range(dims.d_c))
+                for r in range(dims.d_hc)]
+        np.testing.assert_allclose(o[0, i], want, rtol=1e-12, atol=1e-13)
