@@ -209,6 +209,45 @@ mla_status_t mla_output_projection_workspace_size(const mla_dims_t* dims, int32_
 mla_status_t mla_output_projection(const mla_dims_t* dims, const void* W_O, const float* o,
                                    int32_t n, void* ws, size_t ws_bytes, float* u, void* stream);
 
+/* Top-k selection over the latent sequence ([notes] version table, V3.2 + DSA row: MLA is
+ * unchanged; an indexer picks top-k positions of the latent sequence and the core attention
+ * runs MLA over them). The indexer itself is not defined by the pages: its scores are the
+ * caller's input, one float32 per cached position.
+ *   scores      [B, score_stride] float32 device, row b valid at positions 0..seq_len[b]-1
+ *               (score_stride >= max_len; 4-byte aligned). Scores must not be NaN.
+ *   seq_len     [B] device int32, each in [0, max_len] (others flag MLA_ERR_LENGTH and are
+ *               clamped).
+ *   k           1 .. 2^20.
+ *   sel_pos     [B, k] device int32 (output): the positions of the min(k, seq_len[b]) largest
+ *               scores of sequence b, in increasing position order; equal scores rank the lower
+ *               position first, -0.0 equals +0.0. Entries past sel_count[b] are not written.
+ *   sel_count   [B] device int32 (output): min(k, seq_len[b]).
+ * The selection is exact (a radix select on the scores' bit patterns), so the result does not
+ * depend on the launch configuration. B <= 65535. */
+mla_status_t mla_select_topk(const float* scores, int64_t score_stride, const int32_t* seq_len,
+                             int32_t B, int32_t max_len, int32_t k, int32_t* sel_pos,
+                             int32_t* sel_count, void* stream);
+
+/* Workspace needed by mla_decode_absorbed_sparse for B sequences and k picked rows each. */
+mla_status_t mla_decode_sparse_workspace_size(const mla_dims_t* dims, int32_t B, int32_t k,
+                                              size_t* bytes);
+
+/* Sparse absorbed decode: mla_select_topk on the caller's scores, then mla_decode_absorbed's
+ * computation over the picked rows only, the same picks for every head:
+ *   o_{b,i} = W^UV_i sum_{j in S_b} softmax_{j in S_b}(s_{b,i,j}) c^KV_j,  |S_b| = min(k, seq_len[b]).
+ * q_c, q_r, cache, seq_len, max_len, o and the weights are as for mla_decode_absorbed; scores,
+ * score_stride and k as for mla_select_topk. The picked rows are copied into ws (packed per
+ * sequence) and decoded there, so the cache is only read. Rows whose cache index
+ * seq_base[b] + position falls outside [0, capacity) flag MLA_ERR_CAPACITY and read as zero.
+ * On the tensor-core path (mla_fast_path(dims) == 1), with k >= seq_len[b] for every b, the
+ * output equals mla_decode_absorbed's bit for bit. */
+mla_status_t mla_decode_absorbed_sparse(const mla_dims_t* dims, const mla_weights_t* w,
+                                        const void* q_c, const void* q_r,
+                                        const mla_cache_t* cache, const int32_t* seq_len,
+                                        int32_t B, int32_t max_len, const float* scores,
+                                        int64_t score_stride, int32_t k, void* ws,
+                                        size_t ws_bytes, float* o, void* stream);
+
 /* Scratch capacity of mla_decode_absorbed_static, in bytes (32 MiB). */
 #define MLA_STATIC_WS_BYTES (32u << 20)
 
@@ -221,11 +260,16 @@ mla_status_t mla_output_projection(const mla_dims_t* dims, const void* W_O, cons
  * loads the library holds that array until the process exits. The caller still provides
  * q_c, q_r, the cache, seq_len and the output o.
  *  - Problems whose workspace (mla_decode_workspace_size) exceeds MLA_STATIC_WS_BYTES are
- *    rejected with MLA_ERR_WORKSPACE before any launch.
+ *    rejected with MLA_ERR_WORKSPACE before any launch. At the V2 widths in bf16 the workspace
+ *    depends on B alone: up to 31 sequences fit, whatever their lengths. On the SIMT path
+ *    (other widths, fp32) it also grows with max_len.
  *  - The first call on a device looks up the array's device address (once per device, with
- *    that device current); make that first call before any stream capture begins.
+ *    that device current); make that first call before any stream capture begins. The address
+ *    is kept for the life of the process: after the device is reset (cudaDeviceReset, or the
+ *    teardown of its primary context) this entry point must not be called again.
  *  - All calls share the one array, which keeps the previous call's contents; the decode
- *    kernels overwrite every scratch byte they read, so nothing needs clearing. Calls whose
+ *    kernels write every scratch byte they later read within the same call (partial results,
+ *    their (m, l) and each sequence's slot range), so nothing needs clearing. Calls whose
  *    kernels overlap on the GPU (several streams, several host threads) race on the array:
  *    serialise them.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */

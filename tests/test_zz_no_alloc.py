@@ -19,10 +19,10 @@ from helpers import assert_close
 pytestmark = pytest.mark.gpu
 
 
-def _setup(lens, index0):
+def _setup(lens, index0, model=None):
     dims = mi.V2
-    W = mi.weights(dims, "bf16")
-    model = host.DeviceModel.upload(dims, "bf16", W)
+    if model is None:
+        model = host.DeviceModel.upload(dims, "bf16", mi.weights(dims, "bf16"))
     base = mi.packed_layout(lens, guard=2)
     cap = int(base[-1] + lens[-1] + 2)
     cache = host.LatentCache(dims, "bf16", base, cap)
@@ -33,6 +33,18 @@ def _setup(lens, index0):
     q_r = host.to_device(mi.aux_normal((len(lens), dims.n_h, dims.d_hr), index=index0 + 2,
                                        dtype="bf16"), "bf16")
     return model, cache, q_c, q_r
+
+
+def _static_vs_workspace(model, cache, q_c, q_r, lens, tol="bf16"):
+    step = host.DecodeStep(model, cache, lens)
+    want = step.decode(q_c=q_c, q_r=q_r).clone()
+    assert mla.mla_get_device_status() == 0
+    o = torch.full_like(want, float("nan"))
+    mla.mla_decode_absorbed_static(model.abi_dims, model.abi_weights, q_c, q_r, cache.abi,
+                                   step.seq_len, step.B, step.max_len, o)
+    assert mla.mla_get_device_status() == 0
+    assert_close(o.cpu().numpy().astype(np.float64), want.cpu().numpy().astype(np.float64), tol,
+                 "static-scratch decode")
 
 
 def test_static_scratch_decode_matches_workspace_decode_on_two_calls():
@@ -63,3 +75,30 @@ def test_static_scratch_refuses_problems_above_its_capacity():
                                        seq_len, B, max_len, o)
     assert ei.value.status == 7
     assert torch.count_nonzero(o) == 0
+
+
+def test_static_scratch_large_spanning_call_then_small_call():
+    """The array keeps the previous call's contents. A 31-sequence call whose work split crosses
+    sequence boundaries (one long sequence and thirty short ones: many partial slots), then a
+    3-sequence call that uses few: the second must not read anything the first left behind."""
+    lens_big = [74 * 48 * 3] + [5] * 30
+    model, cache, q_c, q_r = _setup(lens_big, 530)
+    _static_vs_workspace(model, cache, q_c, q_r, lens_big)
+    lens_small = [700, 1, 96]
+    _, cache2, q_c2, q_r2 = _setup(lens_small, 540, model)
+    _static_vs_workspace(model, cache2, q_c2, q_r2, lens_small)
+
+
+def test_static_scratch_tiny_fp32_call():
+    """The SIMT path (fp32, other widths) through the same array."""
+    dims = mi.TINY
+    W = mi.weights(dims, "f32")
+    model = host.DeviceModel.upload(dims, "f32", W)
+    lens = [65, 9]
+    base = mi.packed_layout(lens)
+    cap = int(sum(lens))
+    cache = host.LatentCache(dims, "f32", base, cap)
+    cache.rows.copy_(host.to_device(mi.aux_normal((cap, dims.row), index=550), "f32"))
+    q_c = host.to_device(mi.aux_normal((2, dims.n_h, dims.d_hc), index=551), "f32")
+    q_r = host.to_device(mi.aux_normal((2, dims.n_h, dims.d_hr), index=552), "f32")
+    _static_vs_workspace(model, cache, q_c, q_r, lens, tol="f32")
