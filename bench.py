@@ -545,10 +545,11 @@ def run_ours(args, rank, world, local_rank):
     prefill = None
     if not args.no_prefill:
         prefill = run_prefill(args, dev, peaks, flush)
-    out_proj = query_variants = None
+    out_proj = query_variants = sparse = None
     if not args.no_extra_configs:
         out_proj = run_output_projection(args, dev, peaks, flush)
         query_variants = run_query_variants(args, dev, peaks, flush)
+        sparse = run_sparse_decode(args, dev, peaks, flush)
 
     if rank == 0:
         line = {
@@ -561,6 +562,7 @@ def run_ours(args, rank, world, local_rank):
             "step_roofline_frac": main["step_roofline_frac"], "kernels": main["kernels"],
             "three_call_step": main["three_call_step"], "configs": configs, "prefill": prefill,
             "output_projection": out_proj, "query_variants": query_variants,
+            "sparse_decode": sparse,
             "cpu_baseline": main.get("cpu_baseline"), "e2e": main["e2e"],
             "gpu_launches": main["gpu_launches"], "clocks": clocks, "fast_path": main["fast_path"],
             "build": build_info(),
@@ -655,6 +657,70 @@ def run_query_variants(args, dev, peaks, flush):
                          "kernels_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in per.items()}}
         out["n%d" % n] = res
     del model, W_UQK
+    torch.cuda.empty_cache()
+    return out
+
+
+SPARSE_CASES = (("v2_decode_b16_l4096", 2048), ("v2_decode_b1_l131072", 2048))
+
+
+def run_sparse_decode(args, dev, peaks, flush):
+    """Top-k sparse decode (mla_decode_absorbed_sparse: selection on the index scores, gather of
+    the picked rows, absorbed decode over them) on two decode workloads with k = 2048. The
+    algorithmic bytes are the scores (4 B per cached position), the picked rows (1152 B each),
+    W^UK and W^UV, q and o; the gather's copy is not counted. Synthetic N(0,1) rows, queries
+    and scores."""
+    import torch
+    import mla_latent_kv_75_b300 as mla
+    from mla_latent_kv_75_b300 import host
+    d = mi.V2
+    model = host.DeviceModel.upload(d, "bf16", mi.weights(d, "bf16"), dev)
+    dims, w = model.abi_dims, model.abi_weights
+    out = {}
+    for name, k in SPARSE_CASES:
+        wl = mi.workload(name)
+        lens = wl.seq_lens
+        B, max_len = wl.B, max(lens)
+        g = torch.Generator(device=dev)
+        g.manual_seed(5)
+        cache = host.LatentCache(d, "bf16", mi.packed_layout(lens), wl.n_rows, device=dev)
+        cache.rows.copy_(torch.randn(cache.rows.shape, device=dev, generator=g).to(torch.bfloat16))
+        q_c = torch.randn((B, d.n_h, d.d_hc), device=dev, generator=g).to(torch.bfloat16)
+        q_r = torch.randn((B, d.n_h, d.d_hr), device=dev, generator=g).to(torch.bfloat16)
+        scores = torch.randn((B, max_len), device=dev, generator=g)
+        seq_len = torch.tensor(lens, dtype=torch.int32, device=dev)
+        ws_bytes = mla.mla_decode_sparse_workspace_size(dims, B, k)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        o = torch.empty((B, d.n_h, d.d_hc), dtype=torch.float32, device=dev)
+        c = cache.abi
+        call = lambda: mla.mla_decode_absorbed_sparse(dims, w, q_c, q_r, c, seq_len, B, max_len,
+                                                      scores, max_len, k, ws, ws_bytes, o)
+        for _ in range(3):
+            flush()
+            call()
+        assert mla.mla_get_device_status() == 0
+        steps = max(1, min(args.steps, 10))
+        ms, launches = time_steps(call, steps, flush, trace_capacity=8 * steps, hold_ms=0.5)
+        per = {}
+        for kn, t in launches:
+            per.setdefault(kn, []).append(t)
+        us = sum(statistics.mean(v) for v in per.values()) * 1e3
+        picked = sum(min(L, k) for L in lens)
+        row_b = (d.d_c + d.d_hr) * 2
+        alg = (sum(lens) * 4 + picked * row_b + 2 * d.n_h * d.d_hc * d.d_c * 2
+               + B * d.n_h * (d.d_hc + d.d_hr) * 2 + B * d.n_h * d.d_hc * 4)
+        flops = picked * 2 * d.n_h * (d.d_c + d.d_hr + d.d_c)
+        floor_s = max(alg / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+        sel_us = statistics.mean(per["topk_select"]) * 1e3 if "topk_select" in per else None
+        out["%s_k%d" % (name, k)] = {
+            "us": round(us, 2), "call_us": round(statistics.mean(ms) * 1e3, 2),
+            "picked_rows": picked, "alg_bytes": alg, "alg_flops": flops,
+            "roofline_frac": round(floor_s / (us * 1e-6), 4),
+            "select_GB_s": round(sum(lens) * 4 / (sel_us * 1e-6) / 1e9, 1) if sel_us else None,
+            "kernels_us": {kn: round(statistics.mean(v) * 1e3, 2) for kn, v in per.items()}}
+        del cache, ws, scores
+        torch.cuda.empty_cache()
+    del model
     torch.cuda.empty_cache()
     return out
 

@@ -77,6 +77,10 @@ _SIGS = {
     "mla_project_q_premerged": [_PD, _PW, _P, _P, _P, _I, _P, ctypes.c_size_t, _P, _P, _P],
     "mla_output_projection": [_PD, _P, _P, _I, _P, ctypes.c_size_t, _P, _P],
     "mla_decode_step": [_PD, _PW, _P, _P, _PC, _P, _I, _I, _P, ctypes.c_size_t, _P, _P],
+    "mla_select_topk": [_P, ctypes.c_int64, _P, _I, _I, _I, _P, _P, _P],
+    "mla_decode_sparse_workspace_size": [_PD, _I, _I, _SZ],
+    "mla_decode_absorbed_sparse": [_PD, _PW, _P, _P, _PC, _P, _I, _I, _P, ctypes.c_int64, _I, _P,
+                                   ctypes.c_size_t, _P, _P],
     "mla_get_device_status": [_P],
     "mla_fast_path": [_PD],
 }
@@ -235,6 +239,31 @@ def mla_output_projection(dims, W_O, o, n, ws, ws_bytes, u, stream=None) -> None
     _check(_lib.mla_output_projection(ctypes.byref(dims), _ptr(W_O), _ptr(o), int(n), _ptr(ws),
                                       int(ws_bytes), _ptr(u), _stream(stream)),
            "mla_output_projection")
+
+
+def mla_select_topk(scores, score_stride, seq_len, B, max_len, k, sel_pos, sel_count,
+                    stream=None) -> None:
+    _check(_lib.mla_select_topk(_ptr(scores), int(score_stride), _ptr(seq_len), int(B),
+                                int(max_len), int(k), _ptr(sel_pos), _ptr(sel_count),
+                                _stream(stream)), "mla_select_topk")
+
+
+def mla_decode_sparse_workspace_size(dims, B, k) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.mla_decode_sparse_workspace_size(ctypes.byref(dims), int(B), int(k),
+                                                 ctypes.byref(out)),
+           "mla_decode_sparse_workspace_size")
+    return out.value
+
+
+def mla_decode_absorbed_sparse(dims, weights, q_c, q_r, cache, seq_len, B, max_len, scores,
+                               score_stride, k, ws, ws_bytes, o, stream=None) -> None:
+    _check(_lib.mla_decode_absorbed_sparse(ctypes.byref(dims), ctypes.byref(weights), _ptr(q_c),
+                                           _ptr(q_r), ctypes.byref(cache), _ptr(seq_len),
+                                           int(B), int(max_len), _ptr(scores),
+                                           int(score_stride), int(k), _ptr(ws), int(ws_bytes),
+                                           _ptr(o), _stream(stream)),
+           "mla_decode_absorbed_sparse")
 
 
 MLA_STATIC_WS_BYTES = 32 << 20

@@ -64,7 +64,7 @@ const char* const kKernelNames[K_NUM_IDS] = {
     "append", "q_down", "q_up", "absorb", "decode_attn", "decode_combine", "token_map",
     "prefill_append", "prefill_q_down", "prefill_q_up", "expand_k", "expand_v", "prefill_attn",
     "decode_merge", "unabsorb", "q_absorb", "down", "out_split", "out_proj", "merge_w",
-    "q_premerged"};
+    "q_premerged", "topk_select", "gather_rows"};
 }  // namespace
 
 void trace_before(int kernel_id, cudaStream_t st) {
@@ -394,6 +394,84 @@ mla_status_t mla_output_projection(const mla_dims_t* d, const void* W_O, const f
   if (need) MLA_TRY(check_ptr(ws));
   if (fast_dims(d)) return tc_output_projection(d, W_O, o, n, ws, u, as_stream(stream));
   return simt_output_projection(d, W_O, o, n, u, as_stream(stream));
+}
+
+namespace {
+// Sparse-decode workspace: picked positions [B, k] int32, their counts [B] int32, the packed
+// cache's row bases [B] int64, the packed rows [B * k, d_c + d_h^R], then the decode workspace
+// of B sequences of at most k rows.
+struct SparseLayout {
+  size_t off_count, off_base, off_rows, off_dec, total;
+};
+SparseLayout sparse_layout(const mla_dims_t* d, int B, int k) {
+  SparseLayout L;
+  const size_t row_bytes = (size_t)(d->d_c + d->d_hr) * elem_bytes(d);
+  L.off_count = align_up((size_t)B * k * 4, 256);
+  L.off_base = L.off_count + align_up((size_t)B * 4, 256);
+  L.off_rows = L.off_base + align_up((size_t)B * 8, 256);
+  L.off_dec = L.off_rows + align_up((size_t)B * k * row_bytes, 256);
+  L.total = L.off_dec + (fast_dims(d) ? tc_decode_ws(d, B) : simt_decode_ws(d, B, k));
+  return L;
+}
+constexpr int32_t kMaxTopK = 1 << 20;
+}  // namespace
+
+mla_status_t mla_select_topk(const float* scores, int64_t score_stride, const int32_t* seq_len,
+                             int32_t B, int32_t max_len, int32_t k, int32_t* sel_pos,
+                             int32_t* sel_count, void* stream) {
+  if (B < 0 || max_len < 0 || k < 1 || k > kMaxTopK || B > 65535) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!scores || !seq_len || !sel_pos || !sel_count || score_stride < max_len)
+    return MLA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(scores) & 3u) || (reinterpret_cast<uintptr_t>(sel_pos) & 3u) ||
+      (reinterpret_cast<uintptr_t>(sel_count) & 3u))
+    return MLA_ERR_MISALIGNED;
+  return select_topk(scores, score_stride, seq_len, B, max_len, k, sel_pos, sel_count, nullptr,
+                     as_stream(stream));
+}
+
+mla_status_t mla_decode_sparse_workspace_size(const mla_dims_t* d, int32_t B, int32_t k,
+                                              size_t* bytes) {
+  MLA_TRY(check_dims(d));
+  if (!bytes || B < 0 || k < 1 || k > kMaxTopK) return MLA_ERR_INVALID_ARG;
+  *bytes = sparse_layout(d, B, k).total;
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_absorbed_sparse(const mla_dims_t* d, const mla_weights_t* w,
+                                        const void* q_c, const void* q_r,
+                                        const mla_cache_t* cache, const int32_t* seq_len,
+                                        int32_t B, int32_t max_len, const float* scores,
+                                        int64_t score_stride, int32_t k, void* ws,
+                                        size_t ws_bytes, float* o, void* stream) {
+  MLA_TRY(check_dims(d));
+  if (!w || !cache || B < 0 || max_len < 0 || k < 1 || k > kMaxTopK || B > 65535)
+    return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!seq_len || !cache->seq_base || cache->capacity < 0 || !scores || score_stride < max_len)
+    return MLA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(scores) & 3u) return MLA_ERR_MISALIGNED;
+  MLA_TRY(check_ptr(q_c));
+  MLA_TRY(check_ptr(q_r));
+  MLA_TRY(check_ptr(w->W_UK));
+  MLA_TRY(check_ptr(w->W_UV));
+  MLA_TRY(check_ptr(o));
+  if (max_len > 0) MLA_TRY(check_ptr(cache->rows));
+  const SparseLayout L = sparse_layout(d, B, k);
+  if (!ws || ws_bytes < L.total) return MLA_ERR_WORKSPACE;
+  MLA_TRY(check_ptr(ws));
+  char* base = (char*)ws;
+  int32_t* sel = reinterpret_cast<int32_t*>(base);
+  int32_t* count = reinterpret_cast<int32_t*>(base + L.off_count);
+  int64_t* pbase = reinterpret_cast<int64_t*>(base + L.off_base);
+  const cudaStream_t st = as_stream(stream);
+  MLA_TRY(select_topk(scores, score_stride, seq_len, B, max_len, k, sel, count, pbase, st));
+  MLA_TRY(gather_rows(d, cache, sel, count, B, k, base + L.off_rows, st));
+  mla_cache_t packed{base + L.off_rows, pbase, (int64_t)B * k};
+  const int kmax = max_len < k ? max_len : k;
+  if (fast_dims(d))
+    return tc_decode(d, w, q_c, q_r, &packed, count, B, kmax, base + L.off_dec, o, st);
+  return simt_decode(d, w, q_c, q_r, &packed, count, B, kmax, base + L.off_dec, o, st);
 }
 
 mla_status_t mla_debug_arm_wait_timeout(int64_t limit_ns) {

@@ -14,14 +14,20 @@
 // (a "pair", on two SMs) share each piece of work: CTA r owns latent columns
 // [256 r, 256 r + 256) of O~. Both CTAs stream the full 576-wide cache tile and compute the
 // same score tile S = [q~ ; q^R] [c ; k^R]^T (K = 576) themselves: handing a score tile to
-// the other SM through distributed shared memory costs more time than recomputing it. The
-// query operand is split between tensor memory (K columns 0..383) and shared memory (K columns
-// 384..575), because the accumulator, the score tile and the whole query do not fit in the
-// 512 tensor-memory columns together. Per 48-row cache tile, per CTA:
+// the other SM through distributed shared memory costs more time than recomputing it. Per
+// 48-row cache tile, per CTA:
 //   TMA     9 boxes of 64 columns x 48 rows into a 3-deep shared-memory ring
-//   MMA     S = Q K^T (36 K-steps of 16) into tensor memory; later O_r += P V_r (3 K-steps)
-//   softmax one thread per head: online softmax in log2 units with lazy rescaling, P in bf16
-// Both CTAs of a pair therefore hold bitwise identical scores and softmax statistics.
+//   MMA     S = Q K^T (36 K-steps of 16) into one of two tensor-memory score buffers; later
+//           O_r += P V_r (3 K-steps) with P read from tensor memory
+//   softmax one thread per head: online softmax in log2 units with lazy rescaling; P in bf16
+//           written over the first 24 columns of its own score buffer
+// Both CTAs of a pair therefore hold bitwise identical scores and softmax statistics. With two
+// score buffers the score MMA of tile t+2 is issued right behind the PV MMA of tile t, so the
+// tensor pipe does not wait for the softmax to read a score tile out before the next one can
+// be computed. Tensor memory: O_r (256 columns), two score buffers (2 x 48), and the query's K
+// columns 0..319 (160 columns of bf16 pairs); K columns 320..575 of the query live in shared
+// memory. The tensor pipe executes one thread's MMAs in issue order, so the score MMA of tile
+// t+2 overwrites P(t) only after the PV MMA of tile t has read it.
 //
 // Work split (see pairs_for): whenever it fits, every pair works inside one sequence (sequence
 // b gets pairs in proportion to its tile count, each a contiguous share of its tiles, and pair
@@ -53,28 +59,30 @@ constexpr int kStages = 3;
 constexpr int kBox = 64 * kTile * 2;   // one TMA box: 64 columns x 48 rows of bf16 (6 KB)
 constexpr int kStageBytes = 9 * kBox;  // the whole 576-wide tile
 constexpr int kQBox = 64 * kHeads * 2; // 64 query columns x 128 heads (16 KB)
-constexpr int kQTmemK = 384;           // query K columns held in tensor memory
-constexpr int kOffQb = 0;              // query K columns 384..575 (3 boxes)
-constexpr int kOffStage = 3 * kQBox;
-constexpr int kPBytes = kHeads * 128;  // P: one 128-byte swizzled row per head (48 used)
-constexpr int kOffP = kOffStage + kStages * kStageBytes;
-constexpr int kOffBar = kOffP + kPBytes;
+constexpr int kQTmemK = 320;           // query K columns held in tensor memory
+constexpr int kQBoxes = (kRowElems - kQTmemK) / 64;  // query boxes in shared memory (4)
+constexpr int kOffQb = 0;              // query K columns 320..575
+constexpr int kOffStage = kQBoxes * kQBox;
+constexpr int kOffBar = kOffStage + kStages * kStageBytes;
 constexpr int kThreads = 224;  // 7 warps: 0 TMA (score-only boxes), 1 MMA, 2..5 softmax, 6 TMA (V boxes)
 constexpr int kSmemUsed = kOffBar + 256;
 constexpr int kSmemBytes = 232448;  // the opt-in maximum; the base is aligned up to 1 KB
 constexpr int kMaxPairs = 80;       // partial slots are sized for at most this many CTA pairs
-static_assert(kBox % 1024 == 0 && kOffStage % 1024 == 0 && kOffP % 1024 == 0, "1 KB alignment");
+static_assert(kBox % 1024 == 0 && kOffStage % 1024 == 0 && kOffBar % 1024 == 0, "1 KB alignment");
+static_assert(kSmemUsed <= kSmemBytes, "shared memory");
+static_assert(kQTmemK % 64 == 0, "the shared-memory query part starts on a box boundary");
 
 // tensor-memory columns
 constexpr uint32_t kColO = 0;    // O_r: 256 fp32 columns
-constexpr uint32_t kColS = 256;  // S tile: 48 fp32 columns
-constexpr uint32_t kColQ = 320;  // Q K-columns 0..383: 192 columns of bf16 pairs
+constexpr uint32_t kColS = 256;  // score buffer i: 48 fp32 columns at kColS + 48 i
+constexpr uint32_t kColQ = 352;  // Q K-columns 0..319: 160 columns of bf16 pairs
+static_assert(kColS + 2 * kTile <= kColQ && kColQ + kQTmemK / 2 == 512, "tensor-memory map");
 
 constexpr float kTau = 8.f;  // lazy rescale threshold (log2 units): p <= 2^8 between rescales
 
 struct Shared {
   uint64_t full[kStages], empty_a[kStages], empty_b[kStages];
-  uint64_t s_full, s_free, p_full, pv_done, q_full, mma_done, never;
+  uint64_t s_full[2], p_full, pv_done, q_full, mma_done, never;
   uint32_t tmem_slot;
   int abort;
   int b0, j0, nt, nospan;
@@ -144,15 +152,6 @@ __device__ __forceinline__ long long pair_start(int p, long long T, int P) {
   return (long long)p * T / P;
 }
 
-// Pair whose tile range contains tile t.
-__device__ __forceinline__ int pair_of(long long t, long long T, int P) {
-  int p = (int)(t * P / T);
-  if (p >= P) p = P - 1;
-  while (p + 1 < P && pair_start(p + 1, T, P) <= t) ++p;
-  while (p > 0 && pair_start(p, T, P) > t) --p;
-  return p;
-}
-
 // Work split of the tiles over the P CTA pairs.
 // Whole-sequence mode, used whenever it fits: sequence b gets k_b = min(n_b, max(1,
 // floor(n_b P / T))) pairs, and pair c of them takes tiles [c n_b / k_b, (c+1) n_b / k_b) of
@@ -220,8 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.empty_a[s], 1);
       mbar_init(&sh.empty_b[s], 1);
     }
-    mbar_init(&sh.s_full, 1);
-    mbar_init(&sh.s_free, 4);
+    mbar_init(&sh.s_full[0], 1);
+    mbar_init(&sh.s_full[1], 1);
     mbar_init(&sh.p_full, 4);
     mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.q_full, 4);
@@ -303,7 +302,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sh.tmem_slot;
   const int nt = sh.nt;
   uint8_t* const qb = smem + kOffQb;
-  uint8_t* const pbuf = smem + kOffP;
 
   if (nt > 0 && (warp == 0 || warp == 6) && lane == 0) {
     // ------------------------------------------------------------- TMA producers
@@ -336,32 +334,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lane of a converged warp; the descriptors are precomputed and the K loops unrolled)
     constexpr uint32_t idesc_s = idesc_f16(128, kTile, 1, 0, 0);
     constexpr uint32_t idesc_o = idesc_f16(128, 256, 1, 0, 1);
+    // cur: the tile whose PV comes next; ncur: the tile whose score MMA comes next (ns)
     Cursor cur{sh.b0, sh.j0, seq_info(seq_len, seq_base, sh.b0, max_len, capacity, false)};
-    int seg = 0;
+    Cursor ncur = cur;
+    int ns = 0, nseg = 0;  // next score tile, and the segment it belongs to
     const uint64_t desc_qb = smem_desc(smem_u32(qb), 16, 1024);
-    const uint64_t desc_p = smem_desc(smem_u32(pbuf), 16, 1024);
     const uint64_t desc_st = smem_desc(smem_u32(smem + kOffStage), 16, 1024);
     const uint64_t desc_v = smem_desc(smem_u32(smem + kOffStage + 4 * rank * kBox), kBox, 1024);
-    auto issue_s = [&](int t) -> bool {
-      const int s = t % kStages;
-      if (!warp_wait(&sh.full[s], (t / kStages) & 1, abort)) return false;
+    // Score MMA of tile ns into buffer ns & 1. A tile that starts a segment first waits for
+    // that segment's query (the softmax loads it once the previous segment's scores are read).
+    auto issue_next_s = [&]() -> bool {
+      if (ns == 0 || ncur.j == 0) {
+        if (ns > 0) ++nseg;
+        if (!warp_wait(&sh.q_full, nseg & 1, abort)) return false;
+      }
+      const int s = ns % kStages;
+      if (!warp_wait(&sh.full[s], (ns / kStages) & 1, abort)) return false;
       tc_fence_after();
       if (elect_one()) {
+        const uint32_t d_s = tmem + kColS + (uint32_t)((ns & 1) * kTile);
         const uint64_t bst = desc_st + (uint64_t)((s * kStageBytes) >> 4);
 #pragma unroll
         for (int ks = 0; ks < 36; ++ks) {
           const uint64_t bdesc = bst + (uint64_t)(((ks >> 2) * kBox + (ks & 3) * 32) >> 4);
           if (ks < kQTmemK / 16)
-            mma_ts(tmem + kColS, tmem + kColQ + ks * 8, bdesc, idesc_s, ks > 0 ? 1u : 0u);
+            mma_ts(d_s, tmem + kColQ + ks * 8, bdesc, idesc_s, ks > 0 ? 1u : 0u);
           else
-            mma_ss(tmem + kColS,
-                   desc_qb + (uint64_t)((((ks - 24) >> 2) * kQBox + (ks & 3) * 32) >> 4), bdesc,
-                   idesc_s, 1u);
+            mma_ss(d_s,
+                   desc_qb + (uint64_t)((((ks - kQTmemK / 16) >> 2) * kQBox + (ks & 3) * 32) >> 4),
+                   bdesc, idesc_s, 1u);
         }
-        mma_commit(&sh.s_full);
+        mma_commit(&sh.s_full[ns & 1]);
         mma_commit(&sh.empty_a[s]);
       }
       __syncwarp();
+      if (++ns < nt) ncur.next(seq_len, seq_base, max_len, capacity);
       return true;
     };
     bool ok = true;
@@ -387,36 +394,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    ok = ok && warp_wait(&sh.q_full, 0, abort);
-    if (ok) {
-      tc_fence_after();
-      ok = issue_s(0);
-    }
+    // two score tiles ahead of the first PV
+    ok = ok && issue_next_s();
+    if (ok && nt > 1) ok = issue_next_s();
     for (int t = 0; ok && t < nt; ++t) {
-      const bool last_in_seg = cur.j + 1 == cur.s.n;
       const bool seg_first = t == 0 || cur.j == 0;  // O starts from zero
-      if (t + 1 < nt && !last_in_seg) {
-        if (!warp_wait(&sh.s_free, t & 1, abort) || !issue_s(t + 1)) break;
-      }
       if (!warp_wait(&sh.p_full, t & 1, abort)) break;
       tc_fence_after();
       if (elect_one()) {
+        const uint32_t a_p = tmem + kColS + (uint32_t)((t & 1) * kTile);
         const uint64_t bv = desc_v + (uint64_t)(((t % kStages) * kStageBytes) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks)
-          mma_ss(tmem + kColO, desc_p + (uint64_t)((ks * 32) >> 4),
-                 bv + (uint64_t)((ks * 2048) >> 4), idesc_o, (!seg_first || ks > 0) ? 1u : 0u);
+          mma_ts(tmem + kColO, a_p + ks * 8, bv + (uint64_t)((ks * 2048) >> 4), idesc_o,
+                 (!seg_first || ks > 0) ? 1u : 0u);
         mma_commit(&sh.empty_b[t % kStages]);
         mma_commit(&sh.pv_done);
       }
       __syncwarp();
-      if (t + 1 < nt && last_in_seg) {
-        ++seg;
-        if (!warp_wait(&sh.q_full, seg & 1, abort) || !warp_wait(&sh.s_free, t & 1, abort))
-          break;
-        tc_fence_after();
-        if (!issue_s(t + 1)) break;
-      }
+      // the score MMA of tile t+2 reuses buffer t & 1: issued after PV(t), it runs after it
+      if (ns < nt && !issue_next_s()) break;
       if (t + 1 < nt) cur.next(seq_len, seq_base, max_len, capacity);
     }
     // every MMA issued by this CTA completes before its tensor memory is freed
@@ -429,25 +426,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = q * 32 + lane;            // head = TMEM lane
     const int ts = threadIdx.x - 64;        // 0..127 among the softmax threads
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    const int sw = h & 7;
 
-    // Query of sequence b: K columns 0..383 into tensor memory (two bf16 per column, one
-    // thread per head), K columns 384..575 into shared memory by TMA.
+    // Query of sequence b: K columns 0..319 into tensor memory (two bf16 per column, one
+    // thread per head), K columns 320..575 into shared memory by TMA.
     auto load_q = [&](int b) {
       if (ts == 0) {
-        mbar_expect_tx(&sh.q_full, 3 * kQBox);
-        tma_load_2d(qb, &tm_qt, &sh.q_full, 384, b * kHeads);
-        tma_load_2d(qb + kQBox, &tm_qt, &sh.q_full, 448, b * kHeads);
-        tma_load_2d(qb + 2 * kQBox, &tm_qr, &sh.q_full, 0, b * kHeads);
+        mbar_expect_tx(&sh.q_full, kQBoxes * kQBox);
+#pragma unroll
+        for (int x = kQTmemK; x < kDC; x += 64)
+          tma_load_2d(qb + ((x - kQTmemK) / 64) * kQBox, &tm_qt, &sh.q_full, x, b * kHeads);
+        tma_load_2d(qb + (kQBoxes - 1) * kQBox, &tm_qr, &sh.q_full, 0, b * kHeads);
       }
-      // all 48 loads in flight at once: the query rows come from L2 and the load latency,
+      // all 40 loads in flight at once: the query rows come from L2 and the load latency,
       // not the bytes, sets the cost of a segment switch
       const uint4* src = reinterpret_cast<const uint4*>(qt + ((int64_t)b * kHeads + h) * kDC);
-      uint4 v[48];
+      constexpr int kVecs = kQTmemK / 8;
+      uint4 v[kVecs];
 #pragma unroll
-      for (int k = 0; k < 48; ++k) v[k] = __ldg(src + k);
+      for (int k = 0; k < kVecs; ++k) v[k] = __ldg(src + k);
 #pragma unroll
-      for (int c = 0; c < 6; ++c) {
+      for (int c = 0; c < kVecs / 8; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -472,14 +470,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = cur.j;
       const int valid = min(kTile, cur.s.L - j * kTile);
       float s[kTile];
-      if (!warp_wait(&sh.s_full, t & 1, abort)) break;
+      const uint32_t col_s = kColS + (uint32_t)((t & 1) * kTile);  // this tile's score buffer
+      if (!warp_wait(&sh.s_full[t & 1], (t >> 1) & 1, abort)) break;
       tc_fence_after();
-      tmem_ld32(lane_base + kColS, *reinterpret_cast<float(*)[32]>(&s[0]));
-      tmem_ld16(lane_base + kColS + 32, &s[32]);
+      tmem_ld32(lane_base + col_s, *reinterpret_cast<float(*)[32]>(&s[0]));
+      tmem_ld16(lane_base + col_s + 32, &s[32]);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.s_free);
 
       // online softmax in log2 units with lazy rescaling
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -506,7 +502,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l_sum = l_sum * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
 
-      // P and O are free once the previous tile's PV has completed
+      // P over the first 24 columns of this tile's own score buffer (already read out), the
+      // A operand of the PV MMA; the previous tile's PV reads the other buffer meanwhile
+      tmem_st16u(lane_base + col_s, *reinterpret_cast<const uint32_t(*)[16]>(&w[0]));
+      tmem_st8u(lane_base + col_s + 16, *reinterpret_cast<const uint32_t(*)[8]>(&w[16]));
+      // O is free once the previous tile's PV has completed
       if (t > 0 && !warp_wait(&sh.pv_done, (t - 1) & 1, abort)) break;
       if (__any_sync(0xffffffffu, alpha != 1.f && !first)) {
         tc_fence_after();
@@ -521,12 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_wait_st();
       }
-      // P -> shared memory, K-major with the 128-byte swizzle
-      uint8_t* prow = pbuf + h * 128;
-#pragma unroll
-      for (int c = 0; c < kTile / 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) =
-            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      tmem_wait_st();
       if (valid < kTile) {
         // rows past the sequence end may hold anything (even NaN): zero them in the V operand
         uint8_t* v0 = smem + kOffStage + (t % kStages) * kStageBytes + 4 * rank * kBox;

@@ -11,7 +11,7 @@ namespace mla {
 enum KernelId : int {
   K_APPEND = 0, K_Q_DOWN, K_Q_UP, K_ABSORB, K_DECODE_ATTN, K_DECODE_COMBINE, K_TOKEN_MAP,
   K_PREFILL_APPEND, K_PREFILL_Q_DOWN, K_PREFILL_Q_UP, K_EXPAND_K, K_EXPAND_V, K_PREFILL_ATTN,
-  K_DECODE_MERGE, K_UNABSORB, K_Q_ABSORB, K_DOWN, K_OUT_SPLIT, K_OUT_PROJ, K_MERGE_W, K_Q_PREMERGED, K_NUM_IDS
+  K_DECODE_MERGE, K_UNABSORB, K_Q_ABSORB, K_DOWN, K_OUT_SPLIT, K_OUT_PROJ, K_MERGE_W, K_Q_PREMERGED, K_TOPK, K_GATHER, K_NUM_IDS
 };
 
 // Launch tracing (host side): while armed, trace_before/trace_after record caller-owned
@@ -92,6 +92,12 @@ mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* 
 mla_status_t tc_decode_latent(const mla_dims_t* d, const mla_weights_t* w, const void* q_t,
                               const void* q_r, const mla_cache_t* cache, const int32_t* seq_len,
                               int B, int max_len, void* ws, float* o, cudaStream_t st);
+// Top-k selection and row gather for the sparse decode (sparse.cu)
+mla_status_t select_topk(const float* scores, int64_t stride, const int32_t* seq_len, int B,
+                         int max_len, int k, int32_t* sel_pos, int32_t* sel_count,
+                         int64_t* packed_base, cudaStream_t st);
+mla_status_t gather_rows(const mla_dims_t* d, const mla_cache_t* cache, const int32_t* sel_pos,
+                         const int32_t* sel_count, int B, int k, void* packed, cudaStream_t st);
 mla_status_t tc_expand(const void* W, int O, const void* latent, int64_t ld_latent, int K, int n,
                        void* y, bool f16_out, int kid, cudaStream_t st);
 

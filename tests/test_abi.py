@@ -103,3 +103,35 @@ def test_zero_sized_calls_are_no_ops():
 def test_wait_timeout_hook_checks_its_limit_on_the_host():
     assert mla.raw_status("mla_debug_arm_wait_timeout", ctypes.c_int64(0)) == 1
     assert mla.raw_status("mla_debug_arm_wait_timeout", ctypes.c_int64(3_000_000_000)) == 1
+
+
+def test_sparse_entry_points_validate_on_the_host():
+    """Argument checks of the top-k selection and the sparse decode happen before any launch:
+    k out of range, a score stride below max_len, misaligned scores, B = 0 as a no-op."""
+    d = v2_dims()
+    w = mla.MlaWeights()
+    cache = mla.MlaCache(None, None, 0)
+    sel = mla.raw_status
+    # k < 1 and k above 2^20
+    assert sel("mla_select_topk", 0x1000, ctypes.c_int64(64), 0x2000, 1, 64, 0, 0x3000, 0x4000,
+               None) == 1
+    assert sel("mla_select_topk", 0x1000, ctypes.c_int64(64), 0x2000, 1, 64, (1 << 20) + 1,
+               0x3000, 0x4000, None) == 1
+    # stride below max_len
+    assert sel("mla_select_topk", 0x1000, ctypes.c_int64(32), 0x2000, 1, 64, 8, 0x3000, 0x4000,
+               None) == 1
+    # scores not 4-byte aligned
+    assert sel("mla_select_topk", 0x1002, ctypes.c_int64(64), 0x2000, 1, 64, 8, 0x3000, 0x4000,
+               None) == 4
+    # nothing to do
+    assert sel("mla_select_topk", None, ctypes.c_int64(0), None, 0, 0, 8, None, None, None) == 0
+    assert sel("mla_decode_absorbed_sparse", ctypes.byref(d), ctypes.byref(w), None, None,
+               ctypes.byref(cache), None, 0, 0, None, ctypes.c_int64(0), 8, None, 0, None,
+               None) == 0
+    assert sel("mla_decode_absorbed_sparse", ctypes.byref(d), ctypes.byref(w), None, None,
+               ctypes.byref(cache), None, 1, 0, None, ctypes.c_int64(0), 0, None, 0, None,
+               None) == 1
+    # workspace: grows with B and k, and holds at least the packed rows
+    a = mla.mla_decode_sparse_workspace_size(d, 16, 2048)
+    b = mla.mla_decode_sparse_workspace_size(d, 16, 4096)
+    assert 16 * 2048 * 1152 < a < b
