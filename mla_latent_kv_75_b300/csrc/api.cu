@@ -231,7 +231,8 @@ mla_status_t mla_decode_absorbed_latent(const mla_dims_t* d, const mla_weights_t
   MLA_TRY(mla_decode_workspace_size(d, B, max_len, &need));
   if (!ws || ws_bytes < need) return MLA_ERR_WORKSPACE;
   MLA_TRY(check_ptr(ws));
-  return tc_decode_latent(d, w, q_t, q_r, cache, seq_len, B, max_len, ws, o, as_stream(stream));
+  return tc_decode_latent(d, w, q_t, q_r, cache, seq_len, B, max_len, ws, o, false,
+                          as_stream(stream));
 }
 
 namespace {
@@ -283,7 +284,8 @@ mla_status_t mla_decode_step(const mla_dims_t* d, const mla_weights_t* w, const 
   MLA_TRY(tc_down(d, w, h, pos, B, cache, wsb + L.off_hi, wsb + L.off_lo, K_DOWN, st));
   void* q_t = wsb + tc_decode_qt_offset(B);
   MLA_TRY(tc_q_absorbed(d, w, wsb + L.off_hi, wsb + L.off_lo, pos, B, q_t, wsb + L.off_qr, st));
-  return tc_decode_latent(d, w, q_t, wsb + L.off_qr, cache, seq_len, B, max_len, ws, o, st);
+  return tc_decode_latent(d, w, q_t, wsb + L.off_qr, cache, seq_len, B, max_len, ws, o, true,
+                          st);
 }
 
 mla_status_t mla_prefill_workspace_size(const mla_dims_t* d, int32_t n_tok, int32_t B,

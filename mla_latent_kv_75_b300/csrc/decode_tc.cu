@@ -207,6 +207,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = blockIdx.x & 1;  // latent half owned by this CTA
   const int P = gridDim.x / 2, p = blockIdx.x / 2;
+  // The merge kernel after this one may be scheduled now: it waits for this grid to complete
+  // before it reads anything written here.
+  griddep_launch();
   // the aligned layout must fit in the allocation (it does when the base is 1 KB aligned)
   if ((smem - smem_raw) + kSmemUsed > kSmemBytes) {
     if (threadIdx.x == 0) flag_status(MLA_ERR_UNSUPPORTED);
@@ -463,6 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     Cursor cur{sh.b0, sh.j0, seq_info(seq_len, seq_base, sh.b0, max_len, capacity, false)};
+    // q~ comes from the kernel before this one (launched with programmatic serialization, this
+    // grid may start early): wait for it. The cache rows and the lengths were complete before
+    // that kernel started, so the TMA producers need no wait.
+    griddep_wait();
     load_q(cur.b);
     float m_used = -INFINITY, l_sum = 0.f;
     int seg_j0 = cur.j;  // first tile of the current segment
@@ -662,6 +669,8 @@ __global__ void __launch_bounds__(kUnThreads, 1)
       tma_load_2d(smem + k * kUnABox, &tm_wuv, &a_full[k], k * 64, i * 128);
     }
   }
+  // the partial results come from the attention kernel (this grid may start before it ends)
+  griddep_wait();
 
   // ---- merge in teams of G warps per sequence
   int G = 1;
@@ -926,12 +935,13 @@ mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* 
   void* qt = (char*)ws + layout(B).off_qt;
   const mla_status_t s = tc_absorb(d, w, q_c, B, qt, K_ABSORB, st);
   if (s != MLA_OK) return s;
-  return tc_decode_latent(d, w, qt, q_r, cache, seq_len, B, max_len, ws, o, st);
+  return tc_decode_latent(d, w, qt, q_r, cache, seq_len, B, max_len, ws, o, true, st);
 }
 
 mla_status_t tc_decode_latent(const mla_dims_t* d, const mla_weights_t* w, const void* q_t,
                               const void* q_r, const mla_cache_t* cache, const int32_t* seq_len,
-                              int B, int max_len, void* ws, float* o, cudaStream_t st) {
+                              int B, int max_len, void* ws, float* o, bool after_q_kernel,
+                              cudaStream_t st) {
   const Layout L = layout(B);
   char* wsb = (char*)ws;
   const __nv_bfloat16* qt = (const __nv_bfloat16*)q_t;
@@ -968,13 +978,16 @@ mla_status_t tc_decode_latent(const mla_dims_t* d, const mla_weights_t* w, const
         return MLA_ERR_CUDA;
     }
     const float scale_log2 = softmax_scale(d) * 1.4426950408889634f;
+    // With the query kernel of the same call right before it, the attention may start early
+    // (programmatic dependent launch): its set-up, work split and first cache loads overlap the
+    // end of that kernel. As the first kernel of a call it starts normally, since then the
+    // kernel before it may have written the cache or the lengths.
     TraceScope ts(K_DECODE_ATTN, st);
-    decode_attn_tc_kernel<<<2 * pairs, kThreads, kSmemBytes, st>>>(
-        tm_rows, tm_qt, tm_qr, qt, seq_len, cache->seq_base,
-        cache->capacity, B, max_len, scale_log2, part, ml, rng,
-        g_test_stall_ns.exchange(0));
-    s = launch_status();
-    if (s != MLA_OK) return s;
+    if (launch_maybe_pdl(decode_attn_tc_kernel, dim3(2 * pairs), dim3(kThreads), kSmemBytes, st,
+                         after_q_kernel, tm_rows, tm_qt, tm_qr, qt, seq_len, cache->seq_base,
+                         cache->capacity, B, max_len, scale_log2, part, ml, rng,
+                         (int64_t)g_test_stall_ns.exchange(0)) != cudaSuccess)
+      return MLA_ERR_CUDA;
   }
 
   // 3. merge the partials of each sequence and apply W^UV_i (o = 0 for empty sequences)
@@ -988,11 +1001,14 @@ mla_status_t tc_decode_latent(const mla_dims_t* d, const mla_weights_t* w, const
   }
   s = unabsorb_setup();
   if (s != MLA_OK) return s;
+  // always after a kernel of the same call; it reads only weights before griddep_wait
   TraceScope ts(K_UNABSORB, st);
-  decode_unabsorb_kernel<<<dim3(kHeads, ceil_div(B, kUnBN)), kUnThreads, kUnSmem, st>>>(
-      tm_wuv, part, ml, rng, B + kMaxPairs, seq_len, cache->seq_base,
-      max_len > 0 ? cache->capacity : 0, B, max_len, o);
-  return launch_status();
+  if (launch_maybe_pdl(decode_unabsorb_kernel, dim3(kHeads, ceil_div(B, kUnBN)), dim3(kUnThreads),
+                       kUnSmem, st, true, tm_wuv, (const float*)part, (const float*)ml,
+                       (const int2*)rng, B + kMaxPairs, seq_len, cache->seq_base,
+                       max_len > 0 ? cache->capacity : (int64_t)0, B, max_len, o) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 }  // namespace mla

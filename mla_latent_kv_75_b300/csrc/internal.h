@@ -89,9 +89,12 @@ mla_status_t tc_decode(const mla_dims_t* d, const mla_weights_t* w, const void* 
                        const void* q_r, const mla_cache_t* cache, const int32_t* seq_len, int B,
                        int max_len, void* ws, float* o, cudaStream_t st);
 // Decode from the absorbed query q~ [B, n_h, d_c] (attention + merge + W^UV): no absorb launch.
+// after_q_kernel: the kernel right before it in the stream is the same call's query kernel
+// (q~ is its output), so the attention may start early (programmatic dependent launch).
 mla_status_t tc_decode_latent(const mla_dims_t* d, const mla_weights_t* w, const void* q_t,
                               const void* q_r, const mla_cache_t* cache, const int32_t* seq_len,
-                              int B, int max_len, void* ws, float* o, cudaStream_t st);
+                              int B, int max_len, void* ws, float* o, bool after_q_kernel,
+                              cudaStream_t st);
 // Top-k selection and row gather for the sparse decode (sparse.cu)
 mla_status_t select_topk(const float* scores, int64_t stride, const int32_t* seq_len, int B,
                          int max_len, int k, int32_t* sel_pos, int32_t* sel_count,

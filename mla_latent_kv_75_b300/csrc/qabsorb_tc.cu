@@ -100,6 +100,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // c^Q comes from the kernel before this one, which may still be running (programmatic
+  // dependent launch): wait for it. Then the attention kernel after this one may be scheduled;
+  // it reads the cache rows that the down-projection wrote, complete once this wait returns.
+  griddep_wait();
+  griddep_launch();
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -299,11 +304,14 @@ mla_status_t launch_qabsorb(const mla_dims_t* d, const mla_weights_t* w, const v
       attr_done[dev] = true;
     }
   }
+  // always right after the c^Q down-projection of the same call: its set-up may overlap the
+  // end of that kernel (programmatic dependent launch); it waits before reading c^Q
   TraceScope ts(K_Q_ABSORB, st);
-  qabsorb_kernel<BN><<<dim3(kH, ceil_div(n, BN)), kThreads, L::kBytes, st>>>(
-      tuq, tqr, thi, tlo, tuk, d->d_cq / 64, pos, n, (__nv_bfloat16*)q_t, (__nv_bfloat16*)q_r,
-      rope_freqs(d));
-  return launch_status();
+  if (launch_maybe_pdl(qabsorb_kernel<BN>, dim3(kH, ceil_div(n, BN)), dim3(kThreads), L::kBytes,
+                       st, true, tuq, tqr, thi, tlo, tuk, d->d_cq / 64, pos, n,
+                       (__nv_bfloat16*)q_t, (__nv_bfloat16*)q_r, rope_freqs(d)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 }  // namespace

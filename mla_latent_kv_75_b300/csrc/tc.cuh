@@ -7,6 +7,8 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace mla {
@@ -345,6 +347,20 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&r)[1
       : "memory");
 }
 
+// Prefetch the line holding `p` into L1 (no completion to wait for).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+// Programmatic dependent launch. griddep_wait: block until the grids this grid depends on have
+// completed and their writes are visible (returns at once for a grid launched without the
+// programmatic-serialization attribute). griddep_launch: let the next grid of the stream, if
+// it was launched with that attribute, be scheduled before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 8 consecutive 32-bit columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
@@ -417,6 +433,26 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
       if (__shfl_sync(0xffffffffu, stop, 0)) return false;
     }
   }
+}
+
+
+// Launch `kern` on `st`; with `pdl` the launch may overlap the end of the previous kernel in the
+// stream (programmatic dependent launch): the kernel then reads nothing that kernel writes
+// before griddep_wait().
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_maybe_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t st, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace tc
