@@ -57,9 +57,10 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
 }
 
 // One CTA computes a 128 x BN output tile (C = 1; mt_cta consecutive m-tiles per CTA) or, in a
-// cluster of C CTAs, a 1/C share of the K range of one tile (split-K). Split-K partial tiles are
-// reduced through distributed shared memory: CTA c of the cluster sums rows
-// [c * 128/C, (c+1) * 128/C) of all C partials and runs the epilogue on them.
+// cluster of C CTAs (2..8, not only powers of two), a 1/C share of the K range of one tile
+// (split-K). Split-K partial tiles are reduced through distributed shared memory: CTA c of the
+// cluster sums the row pairs [c*64/C, (c+1)*64/C) of all C partials (rows stay in pairs, which
+// the RoPE epilogues need) and runs the epilogue on them.
 template <int BN, int kMode, bool kDual, int kMaxStages, class Ep>
 __global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow ring: 2 CTAs/SM
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tm_w0,
@@ -183,6 +184,8 @@ __global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow
   const bool epi = warp >= 2;
   bool ok = true;
   if (epi) {
+    // while the MMAs run: the per-token data the epilogue looks up (positions, row bases)
+    for (int n = n0 + lane; n < min(N, n0 + BN); n += 32) ep.warm(n);
     ok = warp_wait(done, 0, abort);
     tc_fence_after();
   }
@@ -213,15 +216,19 @@ __global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow
     }
   } else {
     // ---------------- split-K: all-to-all reduction of the partial tiles through DSMEM
-    const int R = 128 / C;  // rows reduced by each CTA of the cluster
-    float* recv = reinterpret_cast<float*>(smem);  // [C][R][BN], the ring is drained
+    // CTA c reduces rows [2 * (c*64/C), 2 * ((c+1)*64/C)): at most Rmax rows
+    const int Rmax = 2 * ((64 + C - 1) / C);
+    float* recv = reinterpret_cast<float*>(smem);  // [C][Rmax][BN], the ring is drained
     __syncthreads();
     cluster_sync();  // every CTA of the cluster finished its MMAs: all rings are free
     if (epi && ok) {
-      const int row = q * 32 + lane;
-      const int dst = row / R, rr = row % R;
+      const int row = q * 32 + lane, pr = row >> 1;
+      int dst = pr * C / 64;  // the CTA whose pair range holds pr
+      while (dst + 1 < C && (dst + 1) * 64 / C <= pr) ++dst;
+      while (dst > 0 && dst * 64 / C > pr) --dst;
+      const int rr = row - 2 * (dst * 64 / C);
       const uint32_t base =
-          mapa_shared(smem_u32(recv + ((size_t)cl * R + rr) * BN), (uint32_t)dst);
+          mapa_shared(smem_u32(recv + ((size_t)cl * Rmax + rr) * BN), (uint32_t)dst);
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         float v[32];
@@ -243,14 +250,15 @@ __global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow
     cluster_sync();  // all partial rows have arrived
     if (epi) {
       const int ts = threadIdx.x - 64;
-      for (int e = ts; e < (R / 2) * BN; e += 128) {
+      const int p0 = cl * 64 / C, np = (cl + 1) * 64 / C - p0;  // this CTA's row pairs
+      for (int e = ts; e < np * BN; e += 128) {
         const int pr = e / BN, col = e % BN;
         float v0 = 0.f, v1 = 0.f;
         for (int src = 0; src < C; ++src) {
-          v0 += recv[((size_t)src * R + 2 * pr) * BN + col];
-          v1 += recv[((size_t)src * R + 2 * pr + 1) * BN + col];
+          v0 += recv[((size_t)src * Rmax + 2 * pr) * BN + col];
+          v1 += recv[((size_t)src * Rmax + 2 * pr + 1) * BN + col];
         }
-        const int o = m_first * 128 + cl * R + 2 * pr, n = n0 + col;
+        const int o = m_first * 128 + 2 * (p0 + pr), n = n0 + col;
         if (n < N && o < O) {
           ep(o, n, v0, v1);
           if (o + 1 < O) ep(o + 1, n, v1, v0);
@@ -448,6 +456,13 @@ struct EpAppend {
   __nv_bfloat16* packed;  // [N, pitch] or null
   int d_c;
   RopeFreqs rf;
+  // Before the accumulator is ready: bring token n's position and row base into L1, so that
+  // the epilogue does not wait on the dependent loads seq_idx -> seq_base.
+  __device__ void warm(int n) const {
+    const int si = seq_idx ? __ldg(seq_idx + n) : n;
+    prefetch_l1(seq_base + si);
+    prefetch_l1(pos + n);
+  }
   __device__ void operator()(int o, int n, float v, float vp) const {
     const int p = pos[n];
     if (o >= d_c) {
@@ -496,6 +511,7 @@ struct EpStoreBF16 {
   __nv_bfloat16* hi;
   __nv_bfloat16* lo;  // null: single bf16
   int64_t ld;
+  __device__ void warm(int) const {}
   __device__ void operator()(int o, int n, float v, float) const {
     const __nv_bfloat16 h = __float2bfloat16_rn(v);
     hi[(int64_t)n * ld + o] = h;
@@ -518,6 +534,7 @@ struct EpStoreBF16 {
 struct EpStoreF32 {
   float* y;
   int64_t ld;
+  __device__ void warm(int) const {}
   __device__ void operator()(int o, int n, float v, float) const { y[(int64_t)n * ld + o] = v; }
   __device__ void row32(int o, int nb, int N, const float* v, const float*) const {
     float* p = y + (int64_t)nb * ld + o;
@@ -550,6 +567,7 @@ __global__ void __launch_bounds__(256) split_hi_lo_kernel(const float4* __restri
 struct EpStoreF16 {
   __half* y;
   int64_t ld;
+  __device__ void warm(int) const {}
   __device__ void operator()(int o, int n, float v, float) const {
     y[(int64_t)n * ld + o] = __float2half_rn(v);
   }
@@ -570,6 +588,7 @@ struct EpDown {
   EpAppend app;
   EpStoreBF16 cq;
   int row_end, q_row0;
+  __device__ void warm(int n) const { app.warm(n); }
   __device__ void operator()(int o, int n, float v, float vp) const {
     if (o < row_end)
       app(o, n, v, vp);
@@ -595,6 +614,7 @@ struct EpQuery {
   const int32_t* pos;
   int n_h, d_hc, d_hr;
   RopeFreqs rf;
+  __device__ void warm(int n) const { prefetch_l1(pos + n); }
   __device__ void operator()(int o, int n, float v, float vp) const {
     const int nc = n_h * d_hc;
     if (o < nc) {
@@ -693,16 +713,18 @@ int max_active_clusters(const void* fn, int c, int smem) {
   return n;
 }
 
-// Split-K cluster size: the largest power of two <= kMaxCluster whose clusters (one per output
-// tile) are all resident at once, so the grid runs as one wave, and that leaves every cluster
-// rank at least one K chunk.
-int choose_split(int tiles, int k_chunks, const void* fn, int smem) {
+// Split-K cluster size: the largest size <= kMaxCluster (any size, not only powers of two)
+// whose clusters (one per output tile) are all resident at once, so the grid runs as one wave,
+// that leaves every cluster rank at least one K chunk, and whose reduction buffer
+// (C x Rmax rows x BN fp32) fits in the drained ring of `ring_bytes`.
+int choose_split(int tiles, int k_chunks, int BN, int ring_bytes, const void* fn, int smem) {
   const int sms = sm_count();
   int c = 1;
-  for (int n = 2; n <= kMaxCluster && tiles * n <= sms; n *= 2) {
+  for (int n = 2; n <= kMaxCluster && tiles * n <= sms; ++n) {
     const int per = (k_chunks + n - 1) / n;
-    if (per * (n - 1) >= k_chunks) break;  // the last rank would get no K chunk
-    if (max_active_clusters(fn, n, smem) < tiles) break;
+    if (per * (n - 1) >= k_chunks) continue;  // the last rank would get no K chunk
+    if ((size_t)n * 2 * ((64 + n - 1) / n) * BN * 4 > (size_t)ring_bytes) continue;
+    if (max_active_clusters(fn, n, smem) < tiles) continue;
     c = n;
   }
   return c;
@@ -770,17 +792,19 @@ mla_status_t launch_proj_bn(const ProjArgs& a, const Ep& ep, cudaStream_t st) {
   // split-K kernel of this launch (cluster size chosen against its residency)
   const void* split_fn = (const void*)proj_gemm_kernel<BN, kPlain, false, 8, Ep>;
   int split_smem = (int)ProjSmem<BN, false>::kBytes + 1024;
+  int split_ring = (int)ProjSmem<BN, false>::kBars;
   if constexpr (BN <= 128) {  // hi/lo inputs need MMAs of width 2*BN
     if (a.X2) {
       split_fn = (const void*)proj_gemm_kernel<BN, kPlain, true, 8, Ep>;
       split_smem = (int)ProjSmem<BN, true>::kBytes + 1024;
+      split_ring = (int)ProjSmem<BN, true>::kBars;
     }
   }
   int C = 1;
   if (m_tiles * ceil_div(a.N, BN) * 2 <= sm_count()) {
     mla_status_t es = ensure_smem(split_fn, split_smem);
     if (es != MLA_OK) return es;
-    C = choose_split(m_tiles * ceil_div(a.N, BN), k_chunks, split_fn, split_smem);
+    C = choose_split(m_tiles * ceil_div(a.N, BN), k_chunks, BN, split_ring, split_fn, split_smem);
   }
   const int O = a.W2 ? m01 * 128 + a.O2 : a.O0 + (a.W1 ? a.O1 : 0);
   if (a.W2 && m_tiles * ceil_div(a.N, BN) > sm_count()) return MLA_ERR_UNSUPPORTED;
