@@ -435,7 +435,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-
 // Launch `kern` on `st`; with `pdl` the launch may overlap the end of the previous kernel in the
 // stream (programmatic dependent launch): the kernel then reads nothing that kernel writes
 // before griddep_wait().
