@@ -83,7 +83,17 @@ def _write_build_info() -> None:
             info = {"git": sha.stdout.strip(), "dirty": bool(st.stdout.strip())}
     except Exception:
         pass
-    with open(os.path.join(BUILD, "build_info.json"), "w") as f:
+    path = os.path.join(BUILD, "build_info.json")
+    if info["git"] is None and os.path.exists(path):
+        # a tree without git (a copy of a built checkout): keep the commit recorded by the
+        # build it was copied from; the bench's source hash tells whether the sources match
+        try:
+            prev = json.load(open(path))
+            if prev.get("git"):
+                info = {"git": prev["git"], "dirty": prev.get("dirty"), "rebuilt_without_git": True}
+        except Exception:
+            pass
+    with open(path, "w") as f:
         json.dump(info, f)
 
 
