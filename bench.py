@@ -74,8 +74,8 @@ DECODE_CALL_KERNELS = ("absorb", "decode_attn", "decode_combine", "unabsorb")
 
 
 def build_info():
-    """Source identity of this run: the commit recorded by the library build (the GPU machine gets
-    a snapshot without .git), else the current commit, plus a hash of the CUDA sources."""
+    """Source identity of this run: the commit recorded by the library build (a copy of the
+    tree may run without .git), else the current commit, plus a hash of the CUDA sources."""
     import hashlib
     info = {}
     try:

@@ -70,8 +70,8 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
 
 
 def _write_build_info() -> None:
-    """Record the commit the library was built from (the GPU machine receives the tree without
-    its .git directory); reporting only."""
+    """Record the commit the library was built from, for a copy of the tree that runs
+    without its .git directory; reporting only."""
     import json
     info = {"git": None, "dirty": None}
     try:
