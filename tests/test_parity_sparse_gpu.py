@@ -47,8 +47,8 @@ def _select(scores, lens, k):
 @pytest.mark.parametrize("kind", ["normal", "ties", "extremes"])
 @pytest.mark.parametrize("k", [1, 64, 2048])
 def test_select_topk_is_bit_exact(kind, k):
-    """Lengths around k and the kernel's chunk sizes (4096 positions per compaction round,
-    16384 per histogram round), one long sequence, and an empty one."""
+    """Lengths around k, lengths that leave some CTAs of the cluster with short or empty
+    slices (40000 positions over three CTAs), and an empty sequence."""
     lens = [0, 1, 5, k - 1 if k > 1 else 1, k, k + 1, 3000, 4097, 16385, 40000]
     stride = max(lens) + 3
     scores = _scores(lens, stride, kind, seed=k)
@@ -161,3 +161,16 @@ def test_sparse_decode_tiny_f32_matches_oracle():
                              dims.d_c)
     mr, _ = rel_errors(o.cpu().numpy().astype(np.float64), want)
     assert mr <= TOL["f32"][0], mr
+
+
+def test_select_topk_long_sequence_walks_several_rounds():
+    """150000 positions: eight CTAs of 18750 positions each, walked in two rounds of 16384
+    re-read from L2, against the oracle bit for bit; ties and a short second sequence too."""
+    lens = [150000, 7]
+    k = 2048
+    scores = _scores(lens, max(lens), "ties", seed=21)
+    sel, cnt = _select(scores, lens, k)
+    for b, L in enumerate(lens):
+        want = ref.select_topk(scores[b], L, k)
+        assert cnt[b] == len(want)
+        np.testing.assert_array_equal(sel[b, :cnt[b]], want)
