@@ -99,7 +99,7 @@ topk_select_kernel(const float* __restrict__ scores, int64_t stride,
                    const int32_t* __restrict__ seq_len, int max_len, int k,
                    int32_t* __restrict__ sel_pos, int32_t* __restrict__ sel_count,
                    int64_t* __restrict__ packed_base) {
-  __shared__ uint32_t hist[kSelWarps][256];
+  __shared__ uint32_t hist[2][kSelWarps][256];  // per warp, double-buffered over the passes
   __shared__ uint32_t hist_cta[2][256];  // this CTA's totals, double-buffered over the passes
   __shared__ uint32_t cnt_cta[2];        // this CTA's keys above T and equal to T
   __shared__ uint32_t scan_tmp[kSelWarps + 1];
@@ -140,13 +140,21 @@ topk_select_kernel(const float* __restrict__ scores, int64_t stride,
   };
   if (rounds == 1) load_round(0);
 
+  // barrier over the cluster (over the CTA alone when it is the whole cluster)
+  auto sync_all = [&]() {
+    if (C > 1)
+      cluster_sync();
+    else
+      __syncthreads();
+  };
+
   // ---- radix select
   uint32_t prefix = 0, mask = 0, need = (uint32_t)k;
+  for (int i = tid; i < kSelWarps * 256; i += kSelThreads) (&hist[0][0][0])[i] = 0u;
+  __syncthreads();
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass, buf = pass & 1;
-    for (int i = tid; i < kSelWarps * 256; i += kSelThreads) (&hist[0][0])[i] = 0u;
-    __syncthreads();
 #pragma unroll 1
     for (int r = 0; r < rounds; ++r) {
       if (rounds > 1) load_round(r);
@@ -155,17 +163,19 @@ topk_select_kernel(const float* __restrict__ scores, int64_t stride,
       for (int i = 0; i < kKeysPerThread; ++i) {
         if (i >= R) break;
         if (j0 + i < s1 && (kk[i] & mask) == prefix)
-          atomicAdd(&hist[warp][(kk[i] >> shift) & 255u], 1u);
+          atomicAdd(&hist[buf][warp][(kk[i] >> shift) & 255u], 1u);
       }
     }
     __syncthreads();
     if (tid < 256) {
       uint32_t t = 0;
 #pragma unroll
-      for (int w = 0; w < kSelWarps; ++w) t += hist[w][tid];
+      for (int w = 0; w < kSelWarps; ++w) t += hist[buf][w][tid];
       hist_cta[buf][tid] = t;
     }
-    cluster_sync();  // every CTA's totals of this pass are visible to the cluster
+    // the other histogram buffer (last read in the previous pass) for the next pass
+    for (int i = tid; i < kSelWarps * 256; i += kSelThreads) (&hist[buf ^ 1][0][0])[i] = 0u;
+    sync_all();  // every CTA's totals of this pass are visible to the cluster
     // totals over the cluster, then the bin holding the need-th largest key: lane l of warp 0
     // owns bins 255-8l down to 248-8l (every CTA computes the same answer)
     if (warp == 0) {
@@ -234,7 +244,7 @@ topk_select_kernel(const float* __restrict__ scores, int64_t stride,
     cnt_cta[0] = tot_gt;
     cnt_cta[1] = tot_eq;
   }
-  cluster_sync();
+  sync_all();
   if (warp == 0) {  // lane rk < c reads CTA rk's counts; a warp sum adds them
     uint32_t g = 0, e = 0;
     if (lane < c) {
@@ -283,7 +293,7 @@ topk_select_kernel(const float* __restrict__ scores, int64_t stride,
     gt_before += rt & 0xffffu;
     eq_before += rt >> 16;
   }
-  cluster_sync();  // no CTA leaves while another may still read its shared memory
+  if (C > 1) cluster_sync();  // no CTA leaves while another may still read its shared memory
 }
 
 template <int kRowVecs>  // 16-byte vectors per cache row
