@@ -296,7 +296,11 @@ mla_status_t mla_prefill(const mla_dims_t* dims, const mla_weights_t* w, const v
                          mla_cache_t* cache, void* ws, size_t ws_bytes, float* o, void* stream);
 
 /* Synchronises `stream`, then returns and clears the device status word (MLA_OK if no kernel
- * flagged anything), or MLA_ERR_CUDA if the stream reports a CUDA error. */
+ * flagged anything), or MLA_ERR_CUDA if the stream reports a CUDA error.
+ * Debugging aid: with the environment variable MLA_DEBUG set (and not "0") when the library is
+ * first used, every kernel launch outside stream capture is followed by a synchronisation of
+ * its stream, and a CUDA error or a latched status is printed on stderr with the kernel's name
+ * (the status word is not cleared). This serialises the host with the GPU. */
 mla_status_t mla_get_device_status(void* stream);
 
 /* Test hook for the bounded device waits (no counterpart on the pages). Arms a one-shot: the

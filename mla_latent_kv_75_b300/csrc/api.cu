@@ -1,6 +1,8 @@
 // C ABI of libmla: argument validation, workspace sizing and dispatch to the kernel files.
 // The operations are those of "MLA前向计算流程" §三分支计算 ①–④ (see include/mla.h).
 #include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -67,13 +69,46 @@ const char* const kKernelNames[K_NUM_IDS] = {
     "q_premerged", "topk_select", "gather_rows"};
 }  // namespace
 
+namespace {
+// MLA_DEBUG (set and not "0", read once per process): after every kernel launch of the library
+// outside stream capture, wait for the stream and report a CUDA error or a latched device
+// status on stderr with the kernel's name. It serialises the host with the GPU: for debugging.
+bool debug_launches() {
+  static const bool on = [] {
+    const char* e = getenv("MLA_DEBUG");
+    return e && *e && strcmp(e, "0") != 0;
+  }();
+  return on;
+}
+thread_local int t_last_kernel = -1;
+
+void debug_check(cudaStream_t st) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return;
+  const char* name =
+      (t_last_kernel >= 0 && t_last_kernel < K_NUM_IDS) ? kKernelNames[t_last_kernel] : "?";
+  const cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    fprintf(stderr, "mla: after %s: %s\n", name, cudaGetErrorString(e));
+    return;
+  }
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) == cudaSuccess && v != 0)
+    fprintf(stderr, "mla: after %s: device status %u (%s)\n", name, v,
+            mla_status_string((mla_status_t)v));
+}
+}  // namespace
+
 void trace_before(int kernel_id, cudaStream_t st) {
+  t_last_kernel = kernel_id;
   if (!g_trace.armed || g_trace.count >= g_trace.n_pairs) return;
   g_trace.ids[g_trace.count] = kernel_id;
   cudaEventRecord((cudaEvent_t)g_trace.events[2 * g_trace.count], st);
 }
 
 void trace_after(cudaStream_t st) {
+  if (debug_launches()) debug_check(st);
   if (!g_trace.armed || g_trace.count >= g_trace.n_pairs) return;
   cudaEventRecord((cudaEvent_t)g_trace.events[2 * g_trace.count + 1], st);
   ++g_trace.count;
