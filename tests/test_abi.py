@@ -135,3 +135,15 @@ def test_sparse_entry_points_validate_on_the_host():
     a = mla.mla_decode_sparse_workspace_size(d, 16, 2048)
     b = mla.mla_decode_sparse_workspace_size(d, 16, 4096)
     assert 16 * 2048 * 1152 < a < b
+
+
+def test_every_kernel_id_has_a_trace_name():
+    """The launch-trace names cover every kernel id the library records, and only those."""
+    names = [mla.mla_kernel_name(i) for i in range(64)]
+    known = [n for n in names if n != "unknown"]
+    assert known == names[:len(known)], "ids are contiguous from 0"
+    assert len(set(known)) == len(known), "names are unique"
+    for n in ("down", "q_absorb", "decode_attn", "unabsorb", "topk_select", "gather_rows",
+              "prefill_attn", "out_proj"):
+        assert n in known
+    assert mla.mla_kernel_name(-1) == "unknown"
