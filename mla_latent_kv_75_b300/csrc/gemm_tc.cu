@@ -84,6 +84,12 @@ __global__ void __launch_bounds__(kThreads, kMaxStages <= 4 ? 2 : 1)  // shallow
   const int n0 = blockIdx.y * BN;
   const bool split = C > 1;
   const int cl = split ? (int)cluster_ctarank() : 0;
+  // The absorb GEMM (the only MN-major use) is followed by the decode attention, launched with
+  // programmatic stream serialization: let it be scheduled now (it waits for this grid to
+  // complete before it reads q~). Measured: releasing every projection GEMM this way slowed the
+  // one-call decode step (the down-projection then lets the fused query kernel in early), so
+  // only this one does.
+  if constexpr (kMode == kGroupedMN) griddep_launch();
   const int m_first = split ? blockIdx.x / C : blockIdx.x * mt_cta;
   const int n_mt = split ? 1 : mt_cta;
   const int kcp = (k_chunks + C - 1) / C;  // K chunks per cluster rank
