@@ -85,10 +85,10 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
 // a CTA holds R <= 32 consecutive positions of each 512 R-position round of its slice, in
 // registers (kept across the passes when the slice is one round, re-read from L2 otherwise).
 //  - radix select, four 8-bit passes, most significant first: every CTA counts the keys that
-//    match the prefix found so far into warp-private shared-memory histograms, totals them
-//    per CTA, and after a cluster barrier every CTA sums the
-//    cluster's totals through distributed shared memory and finds the same bin: the one
-//    holding the `need`-th largest remaining key;
+//    match the prefix found so far into warp-private shared-memory histograms (two buffers,
+//    so that one is cleared while the other is counted), totals them per CTA, and after a
+//    cluster barrier every CTA sums the cluster's totals through distributed shared memory and
+//    finds the same bin: the one holding the `need`-th largest remaining key;
 //  - the result: T, the key of the k-th largest score, and `need`, how many keys equal to T
 //    are picked (the lowest positions among them);
 //  - each CTA counts its keys above T and equal to T; a second cluster exchange gives every
